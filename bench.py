@@ -1,0 +1,393 @@
+"""Benchmark of the deterministic indexer top-k scan on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config S1]
+
+One step = one full scan (the indexer_topk_run call: one kernel) over the workload's
+synthetic inputs. The metric is effective TFLOP/s of useful causal MACs (2 * visible
+(query, key) pairs * H * D per call), with ms per call beside it. Inputs are resident
+in HBM; L2 is flushed between timed steps. Under torchrun each rank runs its own
+replica of the workload (seed + rank) on its own GPU: no collective touches the data
+path; the timing is reduced with a MAX over ranks.
+
+`--impl reference` times the CPU oracle (test infrastructure) on the host cores on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "indexer top-k ms/call and effective TFLOP/s (causal MACs) vs BF16 tensor peak"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "scan_kernel_traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "deterministic_top_key_gb300", "csrc", f)
+                  for f in ("itk_scan.cuh", "itk_ptx.cuh", "itk_host.cu")]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def visible_pairs(wl) -> int:
+    cu_q, cu_k = wl.cu_seqlens_q.astype(np.int64), wl.cu_seqlens_k.astype(np.int64)
+    total = 0
+    for b in range(wl.num_segments):
+        tq, tk = cu_q[b + 1] - cu_q[b], cu_k[b + 1] - cu_k[b]
+        off = wl.q_causal_offsets[b] if wl.q_causal_offsets is not None else tk - tq
+        # query i sees off + i + 1 keys
+        total += int(tq * (off + 1) + tq * (tq - 1) // 2)
+    return total
+
+
+def row_visible(wl) -> np.ndarray:
+    out = np.zeros(wl.T, np.int64)
+    for b in range(wl.num_segments):
+        q0, q1 = int(wl.cu_seqlens_q[b]), int(wl.cu_seqlens_q[b + 1])
+        tq, tk = q1 - q0, int(wl.cu_seqlens_k[b + 1] - wl.cu_seqlens_k[b])
+        off = int(wl.q_causal_offsets[b]) if wl.q_causal_offsets is not None else tk - tq
+        out[q0:q1] = off + np.arange(tq) + 1
+    return out
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}, "fallback"
+
+
+def load_traffic():
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None  # counters were taken on another version of the kernel
+    return d
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_sample(wl, budget_s: float, seed_rows: int = 32):
+    """Time the oracle on a growing, evenly spaced sample of query rows until it has run
+    for at least budget_s / 3 seconds; returns (flops of the sample, seconds, rows, threads)."""
+    import oracle
+
+    oracle.build()
+    p = oracle.Problem(wl.q_bits, wl.k_bits, wl.w, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.top_k, wl.q_causal_offsets)
+    vis = row_visible(wl)
+    n = min(seed_rows, wl.T)
+    while True:
+        rows = np.unique(np.linspace(0, wl.T - 1, n).astype(np.int32))
+        t0 = time.perf_counter()
+        oracle.topk(p, rows=rows)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 3 or len(rows) >= wl.T:
+            flops = 2.0 * float(vis[rows].sum()) * wl.H * wl.D
+            return flops, dt, len(rows), oracle.max_threads()
+        n = min(wl.T, int(n * max(2.0, budget_s / 3 / max(dt, 1e-3))))
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    """The oracle on the host cores: each step scans a bounded sample of the workload."""
+    world, rank, _ = dist_init()
+    if rank != 0:
+        return 0
+    from deterministic_top_key_gb300 import inputs
+
+    wl = inputs.make(args.config, seed=0)
+    # size one step's sample so that all steps together take about a minute
+    per_step_s = max(0.5, min(args.ref_budget, 60.0 / max(args.steps, 1)))
+    flops, dt, nrows, threads = cpu_oracle_sample(wl, 3 * per_step_s)
+    import oracle
+
+    p = oracle.Problem(wl.q_bits, wl.k_bits, wl.w, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.top_k, wl.q_causal_offsets)
+    rows = np.unique(np.linspace(0, wl.T - 1, nrows).astype(np.int32))
+    for _ in range(args.warmup):
+        oracle.topk(p, rows=rows[: max(1, len(rows) // 8)])
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.topk(p, rows=rows)
+        times.append(time.perf_counter() - t0)
+    t = float(np.mean(times))
+    value = flops / t / 1e12
+    full_flops = 2.0 * visible_pairs(wl) * wl.H * wl.D
+    sample = f"{len(rows)} of {wl.T} query rows, evenly spaced ({flops / full_flops:.4%} of the call's MACs)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": full_flops / (value * 1e12) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(wl, world),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl, world):
+    from deterministic_top_key_gb300 import inputs
+
+    return {"workload": f"{wl.name}: {inputs.config(wl.name)['desc']}", "T": wl.T, "Tkv": wl.Tkv, "H": wl.H,
+            "D": wl.D, "top_k": wl.top_k, "segments": wl.num_segments, "l2": "flushed between timed steps",
+            "replicas": world, "inputs": "q,k ~ N(0,1) BF16, w ~ N(0,1)/8, seed 0 (+rank)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="S1")
+    ap.add_argument("--per-config", default="S2,C1,Z2", help="extra configs timed and reported in per_config ('' = none)")
+    ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=20.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+def _to_device(torch, wl, dev):
+    q = torch.from_numpy(wl.q_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    k = torch.from_numpy(wl.k_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    w = torch.from_numpy(wl.w).to(dev)
+    return q, k, w
+
+
+def _measure(binding, torch, wl, dev, steps, warmup, flush_buf):
+    q, k, w = _to_device(torch, wl, dev)
+    plan = binding.indexer_topk_prepare(wl.T, wl.Tkv, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.top_k,
+                                        wl.q_causal_offsets)
+    ws = torch.empty(max(plan.workspace_bytes(), 1), dtype=torch.uint8, device=dev)
+    ids = torch.empty((wl.T, wl.top_k), dtype=torch.int32, device=dev)
+    sc = torch.empty((wl.T, wl.top_k), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush_buf.fill_(1)
+        binding.indexer_topk_run(plan, q, k, w, ids, sc, ws, stream)
+    torch.cuda.synchronize()
+    plan.device_status()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    return plan, (q, k, w, ids, sc, ws), starts, ends, stream
+
+
+def run_ours(args):
+    import torch
+
+    from deterministic_top_key_gb300 import binding, inputs
+
+    world, rank, local = dist_init()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    binding.load()
+
+    peaks, peak_src = load_peaks()
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2_bytes, 256 << 20), dtype=torch.uint8, device=dev)
+
+    wl = inputs.make(args.config, seed=rank)
+    flops = 2.0 * visible_pairs(wl) * wl.H * wl.D
+    plan, bufs, starts, ends, stream = _measure(binding, torch, wl, dev, args.steps, args.warmup, flush_buf)
+    q, k, w, ids, sc, ws = bufs
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    wall0 = time.perf_counter()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush_buf.fill_(i & 0xFF)
+            starts[i].record(stream)
+            binding.indexer_topk_run(plan, q, k, w, ids, sc, ws, stream)
+            ends[i].record(stream)
+        barrier()
+    wall = time.perf_counter() - wall0
+    plan.device_status()
+    per_step_ms = np.array([s.elapsed_time(e) for s, e in zip(starts, ends)])
+    ms = float(per_step_ms.mean())
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * flops / (ms * 1e-3) / 1e12
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq = torch.from_numpy(wl.q_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hk = torch.from_numpy(wl.k_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hw = torch.from_numpy(wl.w).pin_memory()
+        hid = torch.empty(ids.shape, dtype=torch.int32).pin_memory()
+        hsc = torch.empty(sc.shape, dtype=torch.float32).pin_memory()
+        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.warmup + args.steps):
+            flush_buf.fill_(i & 0xFF)
+            if i >= args.warmup:
+                e_s[i - args.warmup].record(stream)
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            w.copy_(hw, non_blocking=True)
+            binding.indexer_topk_run(plan, q, k, w, ids, sc, ws, stream)
+            hid.copy_(ids, non_blocking=True)
+            hsc.copy_(sc, non_blocking=True)
+            if i >= args.warmup:
+                e_e[i - args.warmup].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(e_s, e_e)]))
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = hq.numel() * 2 + hk.numel() * 2 + hw.numel() * 4
+        d2h = hid.numel() * 4 + hsc.numel() * 4
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    # per-config figures (same method; parity-test configs, reported for the roofline)
+    per_config = {}
+    for name in [c for c in args.per_config.split(",") if c and c != args.config]:
+        wl2 = inputs.make(name, seed=rank)
+        f2 = 2.0 * visible_pairs(wl2) * wl2.H * wl2.D
+        plan2, b2, s2, e2, st2 = _measure(binding, torch, wl2, dev, args.steps, args.warmup, flush_buf)
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush_buf.fill_(i & 0xFF)
+            s2[i].record(st2)
+            binding.indexer_topk_run(plan2, *b2, st2)
+            e2[i].record(st2)
+        torch.cuda.synchronize()
+        plan2.device_status()
+        m2 = float(np.mean([a.elapsed_time(b) for a, b in zip(s2, e2)]))
+        tf2 = f2 / (m2 * 1e-3) / 1e12
+        per_config[name] = {"ms": m2, "tflops": tf2, "frac": tf2 / peaks["bf16_tflops"],
+                            "T": wl2.T, "Tkv": wl2.Tkv}
+        plan2.destroy()
+        del b2
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    achieved = flops / (ms * 1e-3) / 1e12
+    traffic = load_traffic()
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
+                "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)" if peak_src == "measured"
+                else "fallback 1.9 PFLOP/s bf16 burst",
+                "traffic": None if traffic is None else traffic["bytes_per_launch_scaled"],
+                "algorithmic_flops_per_launch": flops, "kernel": "indexer_topk_scan_kernel"}
+    if traffic is not None:
+        roofline["traffic_note"] = traffic.get("note", "")
+    flops_s, dt_s, nrows, threads = cpu_oracle_sample(wl, args.cpu_budget)
+    cpu = {"value": flops_s / dt_s / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+           "sample": f"{nrows} of {wl.T} query rows of {wl.name}, evenly spaced; {dt_s:.1f} s"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(wl, world),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(),
+        "gpu_launches": args.steps, "per_config": per_config, "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

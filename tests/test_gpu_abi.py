@@ -1,0 +1,104 @@
+"""C-ABI behaviour on the GPU: argument errors, ticket-block recovery, stream ordering."""
+import numpy as np
+import pytest
+
+from deterministic_top_key_gb300 import inputs
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env(cuda_lib):
+    import torch
+
+    from deterministic_top_key_gb300 import binding
+
+    dev = torch.device("cuda:0")
+    wl = inputs.draw(150, 900, [0, 50, 150], [0, 400, 900], 32, seed=21, kind="int")
+    q, k, w = parity.to_device(wl, dev)
+    import oracle
+
+    ref = oracle.topk(parity.oracle_problem(wl))
+    return binding, torch, dev, wl, (q, k, w), ref
+
+
+def _bufs(torch, dev, wl):
+    ids = torch.empty((wl.T, wl.top_k), dtype=torch.int32, device=dev)
+    sc = torch.empty((wl.T, wl.top_k), dtype=torch.float32, device=dev)
+    return ids, sc
+
+
+def test_argument_errors(env):
+    binding, torch, dev, wl, (q, k, w), _ = env
+    plan = binding.indexer_topk_prepare(wl.T, wl.Tkv, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.top_k)
+    ids, sc = _bufs(torch, dev, wl)
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
+    with pytest.raises(binding.IndexerTopkError) as e:
+        binding.indexer_topk_run(plan, q, k, w, ids, sc, ws[: plan.workspace_bytes() // 2])
+    assert e.value.status == binding.ITK_ERR_WORKSPACE_TOO_SMALL
+    kb = torch.empty(k.numel() + 8, dtype=torch.bfloat16, device=dev)[1:]
+    with pytest.raises(binding.IndexerTopkError) as e:
+        binding.indexer_topk_run(plan, q, kb, w, ids, sc, ws)
+    assert e.value.status == binding.ITK_ERR_MISALIGNED
+    with pytest.raises(binding.IndexerTopkError) as e:
+        binding.indexer_topk_run(plan, q, k, None, ids, sc, ws)
+    assert e.value.status == binding.ITK_ERR_NULL_POINTER
+    plan.destroy()
+    with pytest.raises(binding.IndexerTopkError) as e:
+        binding.indexer_topk_prepare(wl.T, wl.Tkv, wl.cu_seqlens_q, wl.cu_seqlens_k, 4096)
+    assert e.value.status == binding.ITK_ERR_UNSUPPORTED
+
+
+def test_recovery_after_failed_launch(env):
+    """A poisoned ticket block plus a refused launch: the next run zeroes the block first
+    and returns correct rows."""
+    binding, torch, dev, wl, (q, k, w), (r_ids, r_sc) = env
+    plan = binding.indexer_topk_prepare(wl.T, wl.Tkv, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.top_k)
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
+    ids, sc = _bufs(torch, dev, wl)
+    binding.indexer_topk_run(plan, q, k, w, ids, sc, ws)
+    torch.cuda.synchronize()
+    parity.assert_exact(ids.cpu().numpy(), sc.cpu().numpy(), r_ids, r_sc)
+    binding.indexer_topk_debug_inject(plan, 2)  # leave the block nonzero
+    binding.indexer_topk_debug_inject(plan, 1)  # next launch is refused
+    with pytest.raises(binding.IndexerTopkError) as e:
+        binding.indexer_topk_run(plan, q, k, w, ids, sc, ws)
+    assert e.value.status == binding.ITK_ERR_CUDA
+    ids.fill_(5)
+    binding.indexer_topk_run(plan, q, k, w, ids, sc, ws)
+    torch.cuda.synchronize()
+    parity.assert_exact(ids.cpu().numpy(), sc.cpu().numpy(), r_ids, r_sc)
+    plan.device_status()
+    # and the block is left at zero again: another run is still correct
+    ids.fill_(5)
+    binding.indexer_topk_run(plan, q, k, w, ids, sc, ws)
+    torch.cuda.synchronize()
+    parity.assert_exact(ids.cpu().numpy(), sc.cpu().numpy(), r_ids, r_sc)
+    plan.destroy()
+
+
+def test_prepare_and_run_on_ordered_streams(env):
+    binding, torch, dev, wl, (q, k, w), (r_ids, r_sc) = env
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    plan = binding.indexer_topk_prepare(wl.T, wl.Tkv, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.top_k, stream=s1)
+    ev = torch.cuda.Event()
+    ev.record(s1)
+    s2.wait_event(ev)
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
+    ids, sc = _bufs(torch, dev, wl)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        binding.indexer_topk_run(plan, q, k, w, ids, sc, ws, stream=s2)
+    s2.synchronize()
+    parity.assert_exact(ids.cpu().numpy(), sc.cpu().numpy(), r_ids, r_sc)
+    plan.destroy()
+
+
+def test_empty_query_set(env):
+    binding, torch, dev, wl, (q, k, w), _ = env
+    plan = binding.indexer_topk_prepare(0, 10, [0, 0], [0, 10], 8)
+    assert plan.workspace_bytes() == 0
+    e = torch.empty((0, 8), dtype=torch.int32, device=dev)
+    binding.indexer_topk_run(plan, q, k, w, e, e.float(), None)
+    plan.destroy()

@@ -1,0 +1,157 @@
+"""CUDA path vs oracle, through the C ABI, on small and ragged cases."""
+import numpy as np
+import pytest
+
+from deterministic_top_key_gb300 import inputs
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+def run_plan(binding, wl, dev, top_k=None, runs=1):
+    import torch
+
+    q, k, w = parity.to_device(wl, dev)
+    top_k = wl.top_k if top_k is None else top_k
+    plan = binding.indexer_topk_prepare(wl.T, wl.Tkv, wl.cu_seqlens_q, wl.cu_seqlens_k, top_k, wl.q_causal_offsets)
+    ws = torch.empty(max(plan.workspace_bytes(), 1), dtype=torch.uint8, device=dev)
+    outs = []
+    for _ in range(runs):
+        ids = torch.full((wl.T, top_k), 7, dtype=torch.int32, device=dev)
+        sc = torch.full((wl.T, top_k), 7.0, dtype=torch.float32, device=dev)
+        binding.indexer_topk_run(plan, q, k, w, ids, sc, ws)
+        outs.append((ids, sc))
+    torch.cuda.synchronize()
+    plan.device_status()
+    plan.destroy()
+    res = [(i.cpu().numpy(), s.cpu().numpy()) for i, s in outs]
+    return res if runs > 1 else res[0]
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def binding(cuda_lib):
+    from deterministic_top_key_gb300 import binding as b
+
+    return b
+
+
+def test_tiny_integer_bit_exact(binding, dev, oracle_mod):
+    wl = inputs.make("tiny", kind="int")
+    ids, sc = run_plan(binding, wl, dev)
+    r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl))
+    parity.assert_exact(ids, sc, r_ids, r_sc)
+
+
+def test_tiny_random_within_tolerance(binding, dev, oracle_mod):
+    wl = inputs.make("tiny")
+    ids, sc = run_plan(binding, wl, dev)
+    parity.assert_close(ids, sc, wl, np.arange(wl.T))
+
+
+@pytest.mark.parametrize("kind", ["int", "normal"])
+def test_ragged_segments(binding, dev, oracle_mod, kind):
+    # segment sizes leave partial query blocks (nq < 4) and partial key tiles; one empty
+    # query segment; explicit offsets that are neither 0 nor bottom-right
+    tq = [1, 6, 0, 130, 67, 2]
+    tk = [5, 6, 3, 333, 67, 900]
+    offs = [4, 0, 1, 200, 0, 897]
+    cu_q = np.concatenate([[0], np.cumsum(tq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(tk)]).astype(np.int32)
+    wl = inputs.draw(int(cu_q[-1]), int(cu_k[-1]) + 37, cu_q, cu_k, 96, q_causal_offsets=offs, seed=5, kind=kind,
+                     w_dist="uniform")
+    ids, sc = run_plan(binding, wl, dev)
+    if kind == "int":
+        r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl))
+        parity.assert_exact(ids, sc, r_ids, r_sc)
+    else:
+        parity.assert_close(ids, sc, wl, np.arange(wl.T))
+
+
+def test_default_offsets_bottom_right(binding, dev, oracle_mod):
+    tq, tk = [50, 9, 128], [300, 9, 129]
+    cu_q = np.concatenate([[0], np.cumsum(tq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(tk)]).astype(np.int32)
+    wl = inputs.draw(int(cu_q[-1]), int(cu_k[-1]), cu_q, cu_k, 40, seed=8, kind="int")
+    ids, sc = run_plan(binding, wl, dev)
+    r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl))
+    parity.assert_exact(ids, sc, r_ids, r_sc)
+
+
+@pytest.mark.parametrize("top_k", [1, 3, 128, 2048])
+def test_top_k_values(binding, dev, oracle_mod, top_k):
+    wl = inputs.draw(70, 2100, [0, 70], [0, 2100], top_k, seed=2, kind="int")
+    ids, sc = run_plan(binding, wl, dev)
+    r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl))
+    parity.assert_exact(ids, sc, r_ids, r_sc)
+
+
+def _monotone_problem(n_keys, T, direction, top_k):
+    """Scores strictly monotone in the key id (every key enters the candidate buffer when
+    increasing), or all equal (direction 0: pure tie-break)."""
+    H, D = 64, 128
+    q = np.zeros((T, H, D), np.float32)
+    q[:, :, 0] = 1.0
+    k = np.zeros((n_keys, D), np.float32)
+    if direction == 0:
+        k[:, 0] = 1.0
+    else:
+        # distinct positive BF16 values, monotone in the row index
+        base = np.arange(n_keys, dtype=np.uint32) + np.uint32(0x3F80)
+        vals = (base << np.uint32(16)).view(np.float32)
+        k[:, 0] = vals if direction > 0 else vals[::-1]
+    w = np.ones((T, H), np.float32)
+    wl = inputs.Workload("monotone", inputs.f32_to_bf16_bits(q), inputs.f32_to_bf16_bits(k), w,
+                         np.array([0, T], np.int32), np.array([0, n_keys], np.int32), None, top_k)
+    return wl
+
+
+@pytest.mark.parametrize("direction", [1, -1, 0])
+def test_monotone_and_tied_scores(binding, dev, oracle_mod, direction):
+    """Increasing scores and all-equal scores insert every key and force many compactions."""
+    wl = _monotone_problem(9000, 9, direction, 2048)
+    ids, sc = run_plan(binding, wl, dev)
+    r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl))
+    parity.assert_exact(ids, sc, r_ids, r_sc)
+
+
+def test_repeat_runs_bit_identical(binding, dev):
+    wl = inputs.draw(200, 1500, [0, 200], [0, 1500], 256, seed=4, kind="normal")
+    outs = run_plan(binding, wl, dev, runs=3)
+    for ids, sc in outs[1:]:
+        np.testing.assert_array_equal(ids, outs[0][0])
+        np.testing.assert_array_equal(sc.view(np.uint32), outs[0][1].view(np.uint32))
+
+
+def test_rechunked_rows_bit_identical(binding, dev):
+    """Partition independence: the same queries run as one segment or split into two
+    segments (second one on a copy of the keys, matching offset) give identical rows."""
+    wl = inputs.draw(96, 800, [0, 96], [0, 800], 300, seed=9, kind="normal")
+    ids0, sc0 = run_plan(binding, wl, dev)
+    k2 = np.concatenate([wl.k_bits, wl.k_bits])
+    split = inputs.Workload("split", wl.q_bits, k2, wl.w, np.array([0, 37, 96], np.int32),
+                            np.array([0, 800, 1600], np.int32), np.array([704, 741], np.int32), 300)
+    ids1, sc1 = run_plan(binding, split, dev)
+    np.testing.assert_array_equal(sc0.view(np.uint32), sc1.view(np.uint32))
+    np.testing.assert_array_equal(ids0[:37], ids1[:37])
+    np.testing.assert_array_equal(ids0[37:], np.where(ids1[37:] >= 0, ids1[37:] - 800, -1))
+
+
+def test_eager_matches_prepared(binding, dev):
+    import torch
+
+    wl = inputs.draw(130, 600, [0, 130], [0, 600], 64, seed=12, kind="normal")
+    ids0, sc0 = run_plan(binding, wl, dev)
+    q, k, w = parity.to_device(wl, dev)
+    ids1, sc1 = binding.indexer_topk(q, k, w, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.top_k)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(ids1.cpu().numpy(), ids0)
+    np.testing.assert_array_equal(sc1.cpu().numpy().view(np.uint32), sc0.view(np.uint32))
