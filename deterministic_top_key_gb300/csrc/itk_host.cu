@@ -171,9 +171,7 @@ int grid_for(size_t n_units, int sm_count) {
   return static_cast<int>(std::min<size_t>(n_units, static_cast<size_t>(sm_count)));
 }
 
-size_t candidate_bytes(int grid) {
-  return static_cast<size_t>(grid) * itk::kQB * itk::kCap * sizeof(unsigned long long);
-}
+size_t candidate_bytes(int grid) { return static_cast<size_t>(grid) * itk::candidate_bytes_per_cta(); }
 
 // Device block layout shared by the plan and the eager entry: [units | ticket | status].
 struct BlockLayout {

@@ -74,6 +74,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint3
       : "memory");
 }
 
+// Global accesses with an L2 eviction-priority hint (policy from createpolicy below).
+__device__ __forceinline__ void st_hint_u64(unsigned long long* p, unsigned long long v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;" ::"l"(p), "l"(v), "l"(policy) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_hint_u64(const unsigned long long* p, uint64_t policy) {
+  unsigned long long v;
+  asm volatile("ld.global.L2::cache_hint.b64 %0, [%1], %2;" : "=l"(v) : "l"(p), "l"(policy) : "memory");
+  return v;
+}
+// Streaming (evict-first) stores for output rows that are not read again here.
+__device__ __forceinline__ void st_stream_s32(int32_t* p, int32_t v) {
+  asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_stream_f32(float* p, float v) {
+  asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
 // L2 eviction-priority policies for the cache hints above.
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;

@@ -1,7 +1,7 @@
 // The scan kernel: persistent CTAs draw work units from a self-resetting ticket word;
 // each unit (up to 4 consecutive queries of one segment) streams its visible key tiles
-// through a tcgen05 GEMM with the keys as the M side, a fused ReLU * w head reduction and
-// an exact streaming top-k selection.
+// through a tcgen05 GEMM with the keys as the M side, a fused ReLU * w head reduction, a
+// streaming candidate filter, and an exact top-k selection and sort.
 //
 // Operation: flashinfer PR #8691 ("perf(cake_dsa_indexer_det): ticket scheduling on
 // sm_107a, no fill kernel in eager entry"), opening description -- BF16 q/k, FP32 w and
@@ -12,19 +12,43 @@
 // (each running CTA takes the next unit, so a CTA that cannot start does not hold back a
 // second wave) and the TicketWord note (every completed scan leaves the word at zero).
 //
-// CTA layout (320 threads):
-//   warp 0      ticket draws, TMA loads of the Q block and of the K tile ring
-//   warp 1      TMEM allocation, tcgen05.mma issue (one thread)
-//   warps 2..9  epilogue: two groups of four warps; group g owns queries 2g and 2g+1 of
-//               the unit; the four warps of a group cover the 128 TMEM lanes (keys).
+// CTA layout (448 threads, one CTA per SM):
+//   warp 0        ticket draws, TMA loads of the Q block and of the K tile ring
+//   warp 1        TMEM allocation, tcgen05.mma issue (one thread)
+//   warps 2..9    epilogue: two groups of four warps; group g owns queries 2g, 2g+1 of
+//                 the unit; the four warps of a group cover the 128 TMEM lanes (keys).
+//                 Per key tile: scores, candidate filter, appends to the query's
+//                 candidate buffer, histogram of the appended score keys.
+//   warps 10..13  selection group: after a unit's last tile, exact top-k of each query's
+//                 candidates, sort, output rows -- while the other warps already run the
+//                 next unit (candidate buffers and their counts are double-buffered).
 //
-// Score arithmetic (fixed, so the result does not depend on tiling or on which CTA runs
-// a unit): the tensor core forms the FP32 dot products q[t,h,:].k[s,:] over D = 128 in
-// eight K = 16 steps in a fixed order; the epilogue thread that owns key s then computes
-//     acc = 0; for h = 0..63: acc = fma(w[t,h], max(dot_h, 0), acc);  score = acc + 0
+// Score arithmetic (fixed, so a score depends only on q[t], k[s] and w[t], never on
+// tiling, unit or CTA): the tensor core forms the FP32 dot products x_h = q[t,h,:].k[s,:]
+// over D = 128 in eight K = 16 steps in a fixed order; the epilogue thread that owns key
+// s keeps eight partial sums p_m (m = 0..7), p_m = fma(w[t,h], max(x_h, 0), p_m) over
+// h = m, m+8, ..., m+56 in that order, and returns
+//     ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7)) + 0
 // (the "+ 0" turns a -0 into +0). Selection compares (score, id) pairs packed into one
-// 64-bit key (order-preserving score bits above the id), so the order is total and the
-// selected set and its order are unique.
+// 64-bit key (order-preserving score bits above the id bits), so the order is total and
+// the selected set and its order are unique.
+//
+// Candidate filter: a query's candidate buffer holds keys whose score key lies in a bin
+// (top 11 bits of the order-preserving score key) at or above a threshold bin; the
+// threshold bin is the highest bin whose bins-at-or-above hold at least top_k appended
+// keys. It only rises, and every key it rejects is below top_k keys already seen, so the
+// buffer always contains the exact top-k of the keys seen so far. Every count of that
+// histogram is at most the buffer capacity (keys of bins below the threshold are never
+// appended again), so 16-bit counters, two to a word, suffice.
+//
+// Final selection and sort (selection group): the candidates are counted into the same
+// 2048 bins; the bins that reach the first top_k positions are kept, and each kept bin
+// b with c_b keys is spread over c_b sub-buckets by linear position inside the bin, so
+// sub-buckets hold about one key each. Counting, a prefix sum and a scatter put every
+// key into its sub-bucket's slot range, in descending order of sub-bucket; sorting each
+// (tiny) sub-bucket in place finishes the order. Two exact fallbacks handle heavy ties: a
+// radix select inside an oversized sub-bucket that crosses position top_k, and a full
+// bitonic sort when some sub-bucket is large.
 #pragma once
 
 #include <cuda.h>
@@ -42,9 +66,17 @@ constexpr int kN = kQB * kHeads;             // MMA N = 256 (query, head) column
 constexpr int kStages = 3;                   // K tile ring depth
 constexpr int kMaxTopK = 2048;
 constexpr int kCap = 4096;                   // candidate buffer entries per query
-constexpr int kPerThread = kCap / 128;       // candidate entries a group thread holds in compaction
-constexpr int kNumThreads = 320;
+constexpr int kPerThread = kCap / 128;       // entries a 128-thread group holds per thread
+constexpr int kBinShift = 21;                // bin = score key >> 21
+constexpr int kBins = 1 << (32 - kBinShift); // 2048 bins
+constexpr int kStageSlack = 256;             // staging slots past top_k
+constexpr int kBigBucket = 32;               // sub-buckets above this size take the full sort
+constexpr int kNumWarps = 14;
+constexpr int kNumThreads = kNumWarps * 32;
 constexpr int kEpiWarps = 8;
+constexpr int kSelWarps = 4;
+constexpr int kFirstEpiWarp = 2;
+constexpr int kFirstSelWarp = 10;
 constexpr uint32_t kTmemCols = 512;          // two accumulator buffers of 256 columns
 
 constexpr uint32_t kQHalfBytes = kN * 64 * 2;           // 256 rows x 128 B = 32 KB
@@ -55,22 +87,28 @@ constexpr uint32_t kKStageBytes = 2 * kKHalfBytes;       // 32 KB
 // Shared memory layout (offsets from a 1024-byte aligned base).
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
-constexpr uint32_t kOffSort = kOffK + kStages * kKStageBytes;          // 2 groups x 2048 x 8 B
-constexpr uint32_t kOffW = kOffSort + 2 * kMaxTopK * 8;                // 4 queries x 64 floats
-constexpr uint32_t kOffHist = kOffW + kQB * kHeads * 4;                // 2 groups x 256 x 4 B
-constexpr uint32_t kOffThr = kOffHist + 2 * 256 * 4;                   // 4 x u64
-constexpr uint32_t kOffCnt = kOffThr + kQB * 8;                        // 4 x u32
-constexpr uint32_t kOffSel = kOffCnt + kQB * 4;                        // 2 groups x 4 x u32
-constexpr uint32_t kOffUnit = kOffSel + 2 * 4 * 4;                     // 2 slots x int4
+constexpr uint32_t kOffHist = kOffK + kStages * kKStageBytes;          // 4 queries x 1024 words (2 x u16 bins)
+constexpr uint32_t kOffSelBins = kOffHist + kQB * (kBins / 2) * 4;     // 2048 x u32
+constexpr uint32_t kOffSelSub = kOffSelBins + kBins * 4;               // 4096 x u32
+constexpr uint32_t kOffStage = kOffSelSub + kCap * 4;                  // (2048 + 256) x u64
+constexpr uint32_t kOffW = kOffStage + (kMaxTopK + kStageSlack) * 8;   // 4 queries x 64 floats
+constexpr uint32_t kOffRadix = kOffW + kQB * kHeads * 4;               // 3 groups x 256 x u32
+constexpr uint32_t kOffQState = kOffRadix + 3 * 256 * 4;               // 4 queries x 4 x u32
+constexpr uint32_t kOffFinCnt = kOffQState + kQB * 16;                 // 2 buffers x 4 x u32
+constexpr uint32_t kOffSel = kOffFinCnt + 2 * kQB * 4;                 // 3 groups x 8 x u32
+constexpr uint32_t kOffUnit = kOffSel + 3 * 8 * 4;                     // 2 slots x int4
 constexpr uint32_t kOffBar = kOffUnit + 2 * 16;                        // mbarriers
-constexpr uint32_t kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 1;
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;                  // tmem base, abort, fail flags
-constexpr uint32_t kSmemUsed = kOffMisc + 32;
+constexpr uint32_t kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 2 + 1;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;                  // tmem base, abort, flags
+constexpr uint32_t kSmemUsed = kOffMisc + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;                      // slack for 1024-byte alignment
 
-static_assert(kOffK % 1024 == 0 && kKStageBytes % 1024 == 0 && kQHalfBytes % 1024 == 0, "SW128 tiles need 1 KB alignment");
-static_assert(kOffBar % 8 == 0, "mbarrier alignment");
+static_assert(kOffK % 1024 == 0 && kKStageBytes % 1024 == 0 && kQHalfBytes % 1024 == 0,
+              "SW128 tiles need 1 KB alignment");
+static_assert(kOffBar % 8 == 0 && kOffStage % 16 == 0 && kOffW % 16 == 0, "alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kMaxTopK <= kCap - kBlockKeys, "a compaction to top_k must leave room for a tile");
+static_assert(kCap < 65536, "16-bit histogram counters");
 
 struct UnitDesc {
   int32_t q_row0;    // first query row of the unit
@@ -93,8 +131,13 @@ struct ScanParams {
   const float* w;                // [T,64]
   int32_t* out_ids;              // [T,top_k]
   float* out_scores;             // [T,top_k]
-  unsigned long long* cand;      // workspace: gridDim.x x 4 x kCap candidate keys
+  unsigned long long* cand;      // workspace: gridDim.x x 2 x 4 x kCap candidate keys
 };
+
+// Candidate workspace bytes per CTA (two unit buffers of four queries).
+__host__ __device__ constexpr size_t candidate_bytes_per_cta() {
+  return static_cast<size_t>(2) * kQB * kCap * sizeof(unsigned long long);
+}
 
 constexpr uint32_t kStatusTimeout = 10u;  // matches ITK_ERR_DEVICE_TIMEOUT
 
@@ -106,15 +149,20 @@ __device__ __forceinline__ float key_to_float(uint32_t o) {
   const uint32_t b = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
   return __uint_as_float(b);
 }
+__device__ __forceinline__ uint32_t bin_of(unsigned long long key) {
+  return static_cast<uint32_t>(key >> (32 + kBinShift));
+}
 
 struct Bars {
-  uint32_t kfull, kempty, qfull, qempty, accfull, accempty, unitfull, unitempty, mmadone;
+  uint32_t kfull, kempty, qfull, qempty, accfull, accempty, unitfull, unitempty, finfull, finempty, mmadone;
   __device__ uint32_t kf(int s) const { return kfull + 8u * s; }
   __device__ uint32_t ke(int s) const { return kempty + 8u * s; }
   __device__ uint32_t af(int b) const { return accfull + 8u * b; }
   __device__ uint32_t ae(int b) const { return accempty + 8u * b; }
   __device__ uint32_t uf(int s) const { return unitfull + 8u * s; }
   __device__ uint32_t ue(int s) const { return unitempty + 8u * s; }
+  __device__ uint32_t ff(int b) const { return finfull + 8u * b; }
+  __device__ uint32_t fe(int b) const { return finempty + 8u * b; }
 };
 
 __device__ __forceinline__ int n_tiles_of(const int4& u) {
@@ -126,45 +174,73 @@ __device__ __forceinline__ void record_timeout(const ScanParams& p, volatile uin
   atomicOr(p.status, kStatusTimeout | (role << 8));
 }
 
-// ------------------------------------------------------------------ group selection
-// The 128 threads of an epilogue group select, among `n` candidate keys, the `K`
-// largest. Keys are held in registers (entry gtid + 128*r). Radix select from the top
-// byte down; stops as soon as the bucket that holds the K-th largest key is taken whole.
-// Returns `prefix` with #{valid x : x >= prefix} == K.
+// Two FP32 fused multiply-adds in one instruction: (d0, d1) = (a0*b0 + d0, a1*b1 + d1),
+// each rounded once, exactly as two fmaf calls.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 a, b, c;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %5};\n\t"
+      "mov.b64 c, {%0, %1};\n\t"
+      "fma.rn.f32x2 c, a, b, c;\n\t"
+      "mov.b64 {%0, %1}, c;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// Packed 16-bit histogram (two bins per 32-bit word).
+__device__ __forceinline__ uint32_t hist16_get(const uint32_t* h, uint32_t b) {
+  return (h[b >> 1] >> ((b & 1u) * 16u)) & 0xFFFFu;
+}
+__device__ __forceinline__ void hist16_inc(uint32_t* h, uint32_t b) { atomicAdd(&h[b >> 1], 1u << ((b & 1u) * 16u)); }
+
+// ------------------------------------------------------------------ 128-thread groups
 struct GroupCtx {
-  int g;          // group 0/1
-  int gtid;       // 0..127
-  int gwarp;      // 0..3
+  int gtid;        // 0..127
+  int gwarp;       // 0..3
   int lane;
-  uint32_t bar;   // named barrier id
-  uint32_t* hist; // 256 bins
-  uint32_t* sel;  // 4 words of scratch
+  uint32_t bar;    // named barrier id
+  uint32_t* radix; // 256 bins of radix-select scratch
+  uint32_t* sel;   // 8 words of scratch
 };
 
 __device__ __forceinline__ void gsync(const GroupCtx& c) { named_bar_sync(c.bar, 128); }
 
-__device__ unsigned long long group_select(const GroupCtx& c, const unsigned long long (&v)[kPerThread], uint32_t n,
-                                           uint32_t K) {
+// Warp-aggregated append: lanes with `pred` get consecutive slots from *counter.
+__device__ __forceinline__ uint32_t warp_append_slot(bool pred, uint32_t* counter, int lane) {
+  const uint32_t m = __ballot_sync(0xFFFFFFFFu, pred);
+  uint32_t base = 0;
+  if (m) {
+    const int leader = __ffs(m) - 1;
+    if (lane == leader) base = atomicAdd(counter, static_cast<uint32_t>(__popc(m)));
+    base = __shfl_sync(0xFFFFFFFFu, base, leader);
+  }
+  return base + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
+}
+
+// Radix select over keys held in registers (entry r valid iff bit r of `valid`): returns
+// `prefix` with #{valid x : x >= prefix} == K (1 <= K <= number of valid keys). Digits
+// of 8 bits from the top; stops as soon as the bucket holding the K-th largest key is
+// selected whole.
+__device__ unsigned long long group_select(const GroupCtx& c, const unsigned long long (&v)[kPerThread],
+                                           uint32_t valid, uint32_t K) {
   unsigned long long prefix = 0ull;
   uint32_t k_rem = K;
   for (int shift = 56; shift >= 0; shift -= 8) {
-    for (int i = c.gtid; i < 256; i += 128) c.hist[i] = 0u;
+    for (int i = c.gtid; i < 256; i += 128) c.radix[i] = 0u;
     gsync(c);
     const unsigned long long hi_mask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
 #pragma unroll
     for (int r = 0; r < kPerThread; ++r) {
-      const uint32_t idx = c.gtid + 128u * r;
-      if (idx < n && ((v[r] & hi_mask) == (prefix & hi_mask)))
-        atomicAdd(&c.hist[(v[r] >> shift) & 0xFFu], 1u);
+      if (((valid >> r) & 1u) && ((v[r] & hi_mask) == (prefix & hi_mask)))
+        atomicAdd(&c.radix[(v[r] >> shift) & 0xFFu], 1u);
     }
     gsync(c);
     if (c.gwarp == 0) {
-      // lane L scans bins 255-8L .. 248-8L (highest bins first)
       uint32_t cnt[8];
       uint32_t s = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        cnt[i] = c.hist[255 - 8 * c.lane - i];
+        cnt[i] = c.radix[255 - 8 * c.lane - i];
         s += cnt[i];
       }
       uint32_t incl = s;
@@ -189,108 +265,328 @@ __device__ unsigned long long group_select(const GroupCtx& c, const unsigned lon
     }
     gsync(c);
     const uint32_t b = c.sel[0];
-    const uint32_t rem = c.sel[1];
+    k_rem = c.sel[1];
     const uint32_t bucket = c.sel[2];
     prefix |= static_cast<unsigned long long>(b) << shift;
-    k_rem = rem;
-    if (bucket == k_rem) break;  // the whole bucket is selected; uniform across the group
+    if (bucket == k_rem) break;  // uniform across the group
   }
+  gsync(c);  // c.sel may be reused right after
   return prefix;
 }
 
-// Load the candidate buffer into registers (invalid slots are 0, below every real key).
-__device__ __forceinline__ void group_load(const GroupCtx& c, const unsigned long long* buf, uint32_t n,
-                                           unsigned long long (&v)[kPerThread]) {
+// Loads the first n keys of buf into registers (entry gtid + 128*r); returns the valid mask.
+__device__ __forceinline__ uint32_t group_load(const GroupCtx& c, const unsigned long long* buf, uint32_t n,
+                                               unsigned long long (&v)[kPerThread]) {
+  uint32_t valid = 0;
 #pragma unroll
   for (int r = 0; r < kPerThread; ++r) {
     const uint32_t idx = c.gtid + 128u * r;
     v[r] = idx < n ? buf[idx] : 0ull;
+    valid |= (idx < n ? 1u : 0u) << r;
   }
+  return valid;
 }
 
-// Keep the K largest of the n candidates in buf (n > K): afterwards buf[0..K) holds them
-// (in no particular order) and the return value is a key threshold t such that every
-// kept key is >= t and every dropped key is < t.
-__device__ unsigned long long group_compact(const GroupCtx& c, unsigned long long* buf, uint32_t n, uint32_t K,
-                                            uint32_t* s_pos) {
-  unsigned long long v[kPerThread];
-  group_load(c, buf, n, v);
-  if (c.gtid == 0) *s_pos = 0u;
-  const unsigned long long prefix = group_select(c, v, n, K);  // contains barriers after the loads
+// Exclusive prefix sum of a[0..n) in place (n <= 128 * per), 128 threads; returns the total.
+template <int kPer>
+__device__ __forceinline__ uint32_t group_exclusive_scan(const GroupCtx& c, uint32_t* a, uint32_t n) {
+  uint32_t loc[kPer];
+  uint32_t s = 0;
 #pragma unroll
-  for (int r = 0; r < kPerThread; ++r) {
-    const uint32_t idx = c.gtid + 128u * r;
-    const bool keep = idx < n && v[r] >= prefix;
-    const uint32_t m = __ballot_sync(0xFFFFFFFFu, keep);
-    if (m) {
-      uint32_t base = 0;
-      const int leader = __ffs(m) - 1;
-      if (c.lane == leader) base = atomicAdd(s_pos, static_cast<uint32_t>(__popc(m)));
-      base = __shfl_sync(0xFFFFFFFFu, base, leader);
-      if (keep) buf[base + __popc(m & ((1u << c.lane) - 1u))] = v[r];
+  for (int i = 0; i < kPer; ++i) {
+    const uint32_t idx = c.gtid * kPer + i;
+    loc[i] = idx < n ? a[idx] : 0u;
+    s += loc[i];
+  }
+  uint32_t incl = s;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (c.lane >= off) incl += t;
+  }
+  if (c.lane == 31) c.sel[4 + c.gwarp] = incl;
+  gsync(c);
+  uint32_t base = 0, total = 0;
+#pragma unroll
+  for (int wv = 0; wv < 4; ++wv) {
+    const uint32_t x = c.sel[4 + wv];
+    base += wv < c.gwarp ? x : 0u;
+    total += x;
+  }
+  uint32_t run = base + incl - s;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const uint32_t idx = c.gtid * kPer + i;
+    if (idx < n) a[idx] = run;
+    run += loc[i];
+  }
+  gsync(c);
+  return total;
+}
+
+// Epilogue-side compaction of one candidate buffer, used when the next tile could
+// overflow it. First drops the keys below the threshold bin (a streaming pass); if that
+// frees too little (many keys in the threshold bin), keeps exactly the K largest keys and
+// rebuilds the histogram from them. Updates the query state (count, threshold bin, keys
+// at or above it) and the histogram.
+__device__ __forceinline__ void epi_compact(const GroupCtx& c, unsigned long long* buf, uint32_t* qs, uint32_t* hist, uint32_t K,
+                            uint32_t* s_pos, uint64_t pol) {
+  constexpr int kChunk = 16;  // keys per thread per pass
+  const uint32_t n = qs[0];
+  const uint32_t thr = qs[2];
+  if (c.gtid == 0) *s_pos = 0u;
+  gsync(c);
+  for (uint32_t base = 0; base < n; base += 128 * kChunk) {
+    unsigned long long x[kChunk];
+#pragma unroll
+    for (int r = 0; r < kChunk; ++r) {
+      const uint32_t idx = base + c.gtid + 128u * r;
+      x[r] = idx < n ? ld_hint_u64(buf + idx, pol) : 0ull;
+    }
+    gsync(c);  // every key of this chunk is read before any slot of it is rewritten
+#pragma unroll
+    for (int r = 0; r < kChunk; ++r) {
+      const uint32_t idx = base + c.gtid + 128u * r;
+      const bool keep = idx < n && bin_of(x[r]) >= thr;
+      const uint32_t slot = warp_append_slot(keep, s_pos, c.lane);
+      if (keep) st_hint_u64(buf + slot, x[r], pol);
     }
   }
   gsync(c);
-  return prefix;
-}
-
-// Final selection, sort and output of one query row.
-__device__ void group_finish(const GroupCtx& c, const unsigned long long* buf, uint32_t n, uint32_t top_k,
-                             unsigned long long* sbuf, uint32_t* s_pos, int32_t* out_ids, float* out_scores) {
-  unsigned long long v[kPerThread];
-  group_load(c, buf, n, v);
-  const uint32_t keff = n < top_k ? n : top_k;
-  unsigned long long prefix = 0ull;
-  if (c.gtid == 0) *s_pos = 0u;
-  if (n > top_k) {
-    prefix = group_select(c, v, n, top_k);
-  } else {
+  uint32_t m = *s_pos;
+  if (m > static_cast<uint32_t>(kCap - kBlockKeys)) {
+    // Ties crowd the threshold bin: keep exactly the K largest keys.
+    unsigned long long v[kPerThread];
+    const uint32_t valid = group_load(c, buf, m, v);
+    const unsigned long long prefix = group_select(c, v, valid, K);
+    for (int i = c.gtid; i < kBins / 2; i += 128) hist[i] = 0u;
+    if (c.gtid == 0) *s_pos = 0u;
     gsync(c);
-  }
-  // gather the kept keys into shared memory
 #pragma unroll
-  for (int r = 0; r < kPerThread; ++r) {
-    const uint32_t idx = c.gtid + 128u * r;
-    const bool keep = idx < n && v[r] >= prefix;
-    const uint32_t m = __ballot_sync(0xFFFFFFFFu, keep);
-    if (m) {
-      uint32_t base = 0;
-      const int leader = __ffs(m) - 1;
-      if (c.lane == leader) base = atomicAdd(s_pos, static_cast<uint32_t>(__popc(m)));
-      base = __shfl_sync(0xFFFFFFFFu, base, leader);
-      if (keep) sbuf[base + __popc(m & ((1u << c.lane) - 1u))] = v[r];
+    for (int r = 0; r < kPerThread; ++r) {
+      const bool keep = ((valid >> r) & 1u) && v[r] >= prefix;
+      const uint32_t slot = warp_append_slot(keep, s_pos, c.lane);
+      if (keep) {
+        st_hint_u64(buf + slot, v[r], pol);
+        hist16_inc(hist, bin_of(v[r]));
+      }
+    }
+    gsync(c);
+    m = K;
+    if (c.gtid == 0) {
+      qs[2] = bin_of(prefix);
+      qs[3] = K;
     }
   }
-  uint32_t np2 = 2;
-  while (np2 < keff) np2 <<= 1;
+  if (c.gtid == 0) {
+    qs[0] = m;
+    qs[1] = m;
+    qs[3] = m;  // every kept key lies at or above the threshold bin
+  }
   gsync(c);
-  for (uint32_t i = keff + c.gtid; i < np2; i += 128) sbuf[i] = 0ull;
-  gsync(c);
-  // bitonic sort, descending
+}
+
+// Raise a query's threshold bin as far as its histogram allows, by one warp: afterwards
+// thr is the highest bin with at least K appended keys at or above it (it stays put while
+// fewer than K keys have been appended). qs: [0] count, [1] count at the last raise,
+// [2] threshold bin, [3] appended keys at or above the threshold bin.
+__device__ __forceinline__ void warp_raise_threshold(uint32_t* qs, const uint32_t* hist, uint32_t K, int lane) {
+  const uint32_t n = qs[0];
+  uint32_t ge = qs[3] + (n - qs[1]);
+  uint32_t thr = qs[2];
+  if (ge >= K) {
+    while (true) {
+      const uint32_t b = thr + static_cast<uint32_t>(lane);
+      const uint32_t h = b < static_cast<uint32_t>(kBins) ? hist16_get(hist, b) : 0u;
+      uint32_t incl = h;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += t;
+      }
+      // moving the threshold past bins thr..b keeps ge - incl keys at or above it
+      const bool ok = b + 1 < static_cast<uint32_t>(kBins) && incl + K <= ge;
+      const uint32_t adv = static_cast<uint32_t>(__popc(__ballot_sync(0xFFFFFFFFu, ok)));
+      if (adv == 0) break;
+      ge -= __shfl_sync(0xFFFFFFFFu, incl, adv - 1);
+      thr += adv;
+      if (adv < 32) break;
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    qs[1] = n;
+    qs[2] = thr;
+    qs[3] = ge;
+  }
+}
+
+// Bitonic sort (descending) of a[0..np2) in shared memory, np2 a power of two.
+__device__ void group_bitonic_desc(const GroupCtx& c, unsigned long long* a, uint32_t np2) {
   for (uint32_t size = 2; size <= np2; size <<= 1) {
     for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
       for (uint32_t i = c.gtid; i < np2 / 2; i += 128) {
         const uint32_t lo = 2 * i - (i & (stride - 1));
         const uint32_t hi = lo + stride;
         const bool desc = (lo & size) == 0;
-        const unsigned long long a = sbuf[lo];
-        const unsigned long long b = sbuf[hi];
-        if ((a < b) == desc) {
-          sbuf[lo] = b;
-          sbuf[hi] = a;
+        const unsigned long long x = a[lo], y = a[hi];
+        if ((x < y) == desc) {
+          a[lo] = y;
+          a[hi] = x;
         }
       }
       gsync(c);
     }
   }
+}
+
+// Slot-range index (in descending key order) of a kept key. ge[b] counts kept candidates
+// in bins >= b; bin b's keys own sub-buckets [ge[b+1], ge[b]) by linear position inside
+// the bin (higher key first).
+__device__ __forceinline__ uint32_t sub_bucket(const uint32_t* ge, unsigned long long x) {
+  const uint32_t b = bin_of(x);
+  const uint32_t above = b + 1 < static_cast<uint32_t>(kBins) ? ge[b + 1] : 0u;
+  const uint32_t cb = ge[b] - above;
+  const uint32_t frac = static_cast<uint32_t>(x >> 32) & ((1u << kBinShift) - 1u);  // position inside the bin
+  const uint32_t sub = ((frac >> 9) * cb) >> (kBinShift - 9);                       // 0 .. cb-1
+  return above + (cb - 1u - sub);
+}
+
+// Selection group: exact top-k of one query's candidates, sorted by the total order,
+// written as one output row.
+__device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned long long* buf, uint32_t n, uint32_t top_k,
+                           uint32_t* ge, uint32_t* sub, unsigned long long* stage, uint32_t* flags, int32_t* out_ids,
+                           float* out_scores) {
+  unsigned long long v[kPerThread];
+  const uint32_t valid = group_load(c, buf, n, v);
+  const uint32_t keff = n < top_k ? n : top_k;
+  // count the candidates per bin
+  for (int i = c.gtid; i < kBins; i += 128) ge[i] = 0u;
+  if (c.gtid == 0) {
+    flags[0] = kBins - 1;  // first kept bin
+    flags[1] = 0u;         // large sub-bucket seen
+    flags[2] = 0xFFFFFFFFu;  // sub-bucket that crosses top_k and overflows the staging area
+  }
+  gsync(c);
+#pragma unroll
+  for (int r = 0; r < kPerThread; ++r)
+    if ((valid >> r) & 1u) atomicAdd(&ge[bin_of(v[r])], 1u);
+  gsync(c);
+  // ge[b] = candidates in bins >= b (suffix sums, 16 bins per thread, highest bins first)
+  {
+    uint32_t loc[16];
+    uint32_t s = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      loc[i] = ge[kBins - 1 - (16 * c.gtid + i)];
+      s += loc[i];
+    }
+    uint32_t incl = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (c.lane >= off) incl += t;
+    }
+    if (c.lane == 31) c.sel[4 + c.gwarp] = incl;
+    gsync(c);
+    uint32_t run = incl - s;
+#pragma unroll
+    for (int wv = 0; wv < 4; ++wv) run += wv < c.gwarp ? c.sel[4 + wv] : 0u;
+    uint32_t first_kept = kBins - 1;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t b = kBins - 1 - (16 * c.gtid + i);
+      // run = candidates in bins above b; bin b reaches a position below top_k iff run < top_k
+      if (run < top_k) first_kept = b;
+      run += loc[i];
+      ge[b] = run;
+    }
+    atomicMin(&flags[0], first_kept);
+  }
+  gsync(c);
+  const uint32_t tstar = flags[0];
+  const uint32_t m_keep = ge[tstar];  // candidates in kept bins
+  for (uint32_t i = c.gtid; i < m_keep; i += 128) sub[i] = 0u;
+  gsync(c);
+  uint32_t kept = 0;  // bit r: candidate r lies in a kept bin
+#pragma unroll
+  for (int r = 0; r < kPerThread; ++r) {
+    if (((valid >> r) & 1u) && bin_of(v[r]) >= tstar) {
+      kept |= 1u << r;
+      atomicAdd(&sub[sub_bucket(ge, v[r])], 1u);
+    }
+  }
+  gsync(c);
+  group_exclusive_scan<kPerThread>(c, sub, m_keep);  // sub[i] = first slot of sub-bucket i
+  const uint32_t cap = top_k + kStageSlack;
+#pragma unroll
+  for (int r = 0; r < kPerThread; ++r) {
+    if ((kept >> r) & 1u) {
+      const uint32_t pos = atomicAdd(&sub[sub_bucket(ge, v[r])], 1u);
+      if (pos < cap) stage[pos] = v[r];
+    }
+  }
+  gsync(c);
+  // sub[i] is now the end of sub-bucket i; sort every sub-bucket that reaches a slot below
+  // top_k, in place (they hold about one key each)
+  for (uint32_t i = c.gtid; i < m_keep; i += 128) {
+    const uint32_t start = i ? sub[i - 1] : 0u;
+    const uint32_t end = sub[i];
+    if (start >= keff || end - start < 2) continue;
+    if (end > keff && (end > cap || end - start > static_cast<uint32_t>(kBigBucket))) {
+      flags[2] = i;  // the one sub-bucket that crosses position keff, too large to sort here
+      continue;
+    }
+    if (end - start > static_cast<uint32_t>(kBigBucket)) {
+      flags[1] = 1u;
+      continue;
+    }
+    for (uint32_t a = start + 1; a < end; ++a) {
+      const unsigned long long x = stage[a];
+      uint32_t b = a;
+      while (b > start && stage[b - 1] < x) {
+        stage[b] = stage[b - 1];
+        --b;
+      }
+      stage[b] = x;
+    }
+  }
+  gsync(c);
+  const uint32_t over = flags[2];
+  if (over != 0xFFFFFFFFu) {
+    // exact fallback: keep the (keff - start) largest keys of the crossing sub-bucket
+    const uint32_t start = over ? sub[over - 1] : 0u;
+    uint32_t in_b = 0;
+#pragma unroll
+    for (int r = 0; r < kPerThread; ++r)
+      if (((kept >> r) & 1u) && sub_bucket(ge, v[r]) == over) in_b |= 1u << r;
+    const unsigned long long pfx = group_select(c, v, in_b, keff - start);
+    if (c.gtid == 0) flags[3] = start;
+    gsync(c);
+#pragma unroll
+    for (int r = 0; r < kPerThread; ++r) {
+      const bool take = ((in_b >> r) & 1u) && v[r] >= pfx;
+      const uint32_t slot = warp_append_slot(take, &flags[3], c.lane);
+      if (take) stage[slot] = v[r];
+    }
+    if (c.gtid == 0) flags[1] = 1u;  // the refilled range is unsorted
+    gsync(c);
+  }
+  if (flags[1]) {
+    uint32_t np2 = 2;
+    while (np2 < keff) np2 <<= 1;
+    for (uint32_t i = keff + c.gtid; i < np2; i += 128) stage[i] = 0ull;
+    gsync(c);
+    group_bitonic_desc(c, stage, np2);
+  }
   for (uint32_t r = c.gtid; r < top_k; r += 128) {
     if (r < keff) {
-      const unsigned long long x = sbuf[r];
-      out_ids[r] = static_cast<int32_t>(static_cast<uint32_t>(x & 0xFFFFFFFFull));
-      out_scores[r] = key_to_float(static_cast<uint32_t>(x >> 32));
+      const unsigned long long x = stage[r];
+      st_stream_s32(out_ids + r, static_cast<int32_t>(static_cast<uint32_t>(x & 0xFFFFFFFFull)));
+      st_stream_f32(out_scores + r, key_to_float(static_cast<uint32_t>(x >> 32)));
     } else {
-      out_ids[r] = -1;
-      out_scores[r] = -__int_as_float(0x7F800000);
+      st_stream_s32(out_ids + r, -1);
+      st_stream_f32(out_scores + r, -__int_as_float(0x7F800000));
     }
   }
   gsync(c);
@@ -305,15 +601,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  unsigned long long* s_thr = reinterpret_cast<unsigned long long*>(smem + kOffThr);
-  uint32_t* s_cnt = reinterpret_cast<uint32_t*>(smem + kOffCnt);
+  // per-query epilogue state: [j][0] count, [1] count at the last threshold raise,
+  // [2] threshold bin, [3] keys appended at or above the threshold bin
+  uint32_t* s_qs = reinterpret_cast<uint32_t*>(smem + kOffQState);
+  uint32_t* s_fin = reinterpret_cast<uint32_t*>(smem + kOffFinCnt);  // [buffer][query] final counts
   int4* s_unit = reinterpret_cast<int4*>(smem + kOffUnit);
   float* s_w = reinterpret_cast<float*>(smem + kOffW);
   uint32_t* s_misc = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   uint32_t* s_tmem = s_misc + 0;
   volatile uint32_t* s_abort = s_misc + 1;
-  uint32_t* s_gfail = s_misc + 2;  // [2] per-group failure flags
-  uint32_t* s_pos = s_misc + 4;    // [2] per-group compaction cursors
+  uint32_t* s_gfail = s_misc + 2;  // [3] per-group failure flags
+  uint32_t* s_pos = s_misc + 6;    // [2] epilogue-group cursors
+  uint32_t* s_flags = s_misc + 8;  // [4] selection-group flags
 
   const uint32_t bar0 = smem_u32(smem + kOffBar);
   Bars bars;
@@ -325,7 +624,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   bars.accempty = bars.accfull + 16;
   bars.unitfull = bars.accempty + 16;
   bars.unitempty = bars.unitfull + 16;
-  bars.mmadone = bars.unitempty + 16;
+  bars.finfull = bars.unitempty + 16;
+  bars.finempty = bars.finfull + 16;
+  bars.mmadone = bars.finempty + 16;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -338,12 +639,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bars.af(b), 1);
       mbar_init(bars.ae(b), kEpiWarps);
       mbar_init(bars.uf(b), 1);
-      mbar_init(bars.ue(b), 1 + kEpiWarps);
+      mbar_init(bars.ue(b), 1 + kEpiWarps + kSelWarps);
+      mbar_init(bars.ff(b), kEpiWarps);
+      mbar_init(bars.fe(b), kSelWarps);
     }
     mbar_init(bars.mmadone, 1);
-    s_misc[1] = 0u;
-    s_misc[2] = 0u;
-    s_misc[3] = 0u;
+    for (int i = 1; i < 16; ++i) s_misc[i] = 0u;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -408,8 +709,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         ++it;
       }
-      // Drain: make sure no TMA write into this CTA's shared memory is still in flight
-      // (these waits ignore the abort flag but keep their time limit).
+      // Drain: no TMA write into this CTA's shared memory may still be in flight (these
+      // waits ignore the abort flag but keep their time limit).
       for (uint32_t j = (kc > kStages ? kc - kStages : 0); j < kc; ++j)
         mbar_wait(bars.kf(j % kStages), (j / kStages) & 1, nullptr);
       if (qloads > 0) mbar_wait(bars.qfull, (qloads - 1) & 1, nullptr);
@@ -473,140 +774,192 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         mbar_arrive(bars.ue(slot));
         ++it;
       }
-      // Wait until every MMA this thread issued has completed before TMEM is released
-      // (ignores the abort flag, keeps the time limit).
+      // Every MMA this thread issued completes before TMEM is released (ignores the
+      // abort flag, keeps the time limit).
       mma_commit(bars.mmadone);
       mbar_wait(bars.mmadone, 0, nullptr);
     }
-  } else {
+  } else if (warp < kFirstSelWarp) {
     // ---------------------------------------------------------------- epilogue
-    const int ew = warp - 2;
+    const int ew = warp - kFirstEpiWarp;
+    const int g = ew >> 2;
     GroupCtx c;
-    c.g = ew >> 2;
     c.gwarp = ew & 3;
     c.lane = lane;
     c.gtid = c.gwarp * 32 + lane;
-    c.bar = 1 + c.g;
-    c.hist = reinterpret_cast<uint32_t*>(smem + kOffHist) + 256 * c.g;
-    c.sel = reinterpret_cast<uint32_t*>(smem + kOffSel) + 4 * c.g;
-    unsigned long long* sbuf = reinterpret_cast<unsigned long long*>(smem + kOffSort) + kMaxTopK * c.g;
+    c.bar = 1 + g;
+    c.radix = reinterpret_cast<uint32_t*>(smem + kOffRadix) + 256 * g;
+    c.sel = reinterpret_cast<uint32_t*>(smem + kOffSel) + 8 * g;
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int key_lane = quarter * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    unsigned long long* cand_base = p.cand + static_cast<size_t>(blockIdx.x) * kQB * kCap;
+    const uint32_t K = static_cast<uint32_t>(p.top_k);
+    const uint64_t pol_cand = policy_evict_last();
+    uint32_t* hist_g = reinterpret_cast<uint32_t*>(smem + kOffHist) + (2 * g) * (kBins / 2);
 
     uint32_t it = 0, ac = 0;
     while (true) {
-      const int slot = it & 1;
+      const int slot = it & 1;  // also the candidate buffer set of this unit
       // Every decision to leave the loop is taken by the whole group at once (flag set
       // before a group barrier, read after it), so no warp is left waiting at a barrier.
       if (!mbar_wait(bars.uf(slot), (it >> 1) & 1, s_abort)) {
         record_timeout(p, s_abort, 8);
-        atomicOr(&s_gfail[c.g], 1u);
+        atomicOr(&s_gfail[g], 1u);
+      }
+      if (!mbar_wait(bars.fe(slot), ((it >> 1) & 1) ^ 1, s_abort)) {
+        record_timeout(p, s_abort, 9);
+        atomicOr(&s_gfail[g], 1u);
       }
       gsync(c);
-      if (s_gfail[c.g]) break;
+      if (s_gfail[g]) break;
       const int4 unit = s_unit[slot];
       if (unit.x < 0) break;
-      // per-unit state of this group's two queries
+      unsigned long long* cand = p.cand + (static_cast<size_t>(blockIdx.x) * 2 + slot) * kQB * kCap;
       for (int i = c.gtid; i < 2 * kHeads; i += 128) {
-        const int jj = i / kHeads, h = i % kHeads;
-        const int j = 2 * c.g + jj;
+        const int j = 2 * g + i / kHeads, h = i % kHeads;
         s_w[j * kHeads + h] = j < unit.y ? p.w[static_cast<size_t>(unit.x + j) * kHeads + h] : 0.f;
       }
-      if (c.gtid < 2) {
-        s_cnt[2 * c.g + c.gtid] = 0u;
-        s_thr[2 * c.g + c.gtid] = 0ull;
-      }
+      for (int i = c.gtid; i < kBins; i += 128) hist_g[i] = 0u;  // both queries' packed bins
+      if (c.gtid < 8) s_qs[(2 * g) * 4 + c.gtid] = 0u;
       gsync(c);
       const int nt = n_tiles_of(unit);
       bool failed = false;
       for (int tile = 0; tile < nt; ++tile, ++ac) {
         const int ab = ac & 1;
         if (!mbar_wait(bars.af(ab), (ac >> 1) & 1, s_abort)) {
-          record_timeout(p, s_abort, 9);
-          atomicOr(&s_gfail[c.g], 1u);
+          record_timeout(p, s_abort, 10);
+          atomicOr(&s_gfail[g], 1u);
         }
-        gsync(c);
-        if (s_gfail[c.g]) {
+        gsync(c);  // (A) also: every append of the previous tile is done
+        if (s_gfail[g]) {
           failed = true;
           break;
         }
-        tc_fence_after_sync();
-        const int jl = tile * kBlockKeys + key_lane;  // local key index within the segment
+        // make room when this tile's appends could overflow a buffer (uniform decision;
+        // uses the threshold of the last raise)
 #pragma unroll 1
         for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * c.g + jj;
-          if (j >= unit.y) continue;  // uniform across the group
-          uint32_t r0[32], r1[32];
-          const uint32_t col = static_cast<uint32_t>(ab * kN + j * kHeads);
-          tmem_ld32(lane_addr + col, r0);
-          tmem_ld32(lane_addr + col + 32, r1);
-          tmem_ld_wait();
-          const float4* wv = reinterpret_cast<const float4*>(s_w + j * kHeads);
-          float acc = 0.f;
+          const int j = 2 * g + jj;
+          if (j < unit.y && s_qs[j * 4] > static_cast<uint32_t>(kCap - kBlockKeys))
+            epi_compact(c, cand + static_cast<size_t>(j) * kCap, s_qs + j * 4, hist_g + jj * (kBins / 2), K,
+                        &s_pos[g], pol_cand);
+        }
+        // warp jj raises query 2g+jj's threshold from the counts of the tiles so far,
+        // while the scores of this tile are computed
+        if (c.gwarp < 2 && 2 * g + c.gwarp < unit.y)
+          warp_raise_threshold(s_qs + (2 * g + c.gwarp) * 4, hist_g + c.gwarp * (kBins / 2), K, lane);
+        tc_fence_after_sync();
+        const int jl = tile * kBlockKeys + key_lane;  // local key index within the segment
+        uint32_t key32[2] = {0u, 0u};
 #pragma unroll
-          for (int h4 = 0; h4 < 8; ++h4) {
-            const float4 w4 = wv[h4];
-            acc = fmaf(w4.x, fmaxf(__uint_as_float(r0[4 * h4 + 0]), 0.f), acc);
-            acc = fmaf(w4.y, fmaxf(__uint_as_float(r0[4 * h4 + 1]), 0.f), acc);
-            acc = fmaf(w4.z, fmaxf(__uint_as_float(r0[4 * h4 + 2]), 0.f), acc);
-            acc = fmaf(w4.w, fmaxf(__uint_as_float(r0[4 * h4 + 3]), 0.f), acc);
-          }
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = 2 * g + jj;
+          if (j < unit.y) {  // uniform across the group
+            uint32_t x[64];
+            const uint32_t col = static_cast<uint32_t>(ab * kN + j * kHeads);
+            tmem_ld32(lane_addr + col, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+            tmem_ld32(lane_addr + col + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+            tmem_ld_wait();
+            const float4* wv = reinterpret_cast<const float4*>(s_w + j * kHeads);
+            float ps[8];
 #pragma unroll
-          for (int h4 = 0; h4 < 8; ++h4) {
-            const float4 w4 = wv[8 + h4];
-            acc = fmaf(w4.x, fmaxf(__uint_as_float(r1[4 * h4 + 0]), 0.f), acc);
-            acc = fmaf(w4.y, fmaxf(__uint_as_float(r1[4 * h4 + 1]), 0.f), acc);
-            acc = fmaf(w4.z, fmaxf(__uint_as_float(r1[4 * h4 + 2]), 0.f), acc);
-            acc = fmaf(w4.w, fmaxf(__uint_as_float(r1[4 * h4 + 3]), 0.f), acc);
-          }
-          const float score = acc + 0.0f;
-          const bool vis = jl <= unit.w + j;
-          const unsigned long long key = (static_cast<unsigned long long>(ord_key(score)) << 32) |
-                                         static_cast<uint32_t>(unit.z + jl);
-          const bool ins = vis && key >= s_thr[j];
-          const uint32_t m = __ballot_sync(0xFFFFFFFFu, ins);
-          if (m) {
-            uint32_t base = 0;
-            const int leader = __ffs(m) - 1;
-            if (lane == leader) base = atomicAdd(&s_cnt[j], static_cast<uint32_t>(__popc(m)));
-            base = __shfl_sync(0xFFFFFFFFu, base, leader);
-            if (ins) cand_base[static_cast<size_t>(j) * kCap + base + __popc(m & ((1u << lane) - 1u))] = key;
+            for (int m = 0; m < 8; ++m) ps[m] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {  // heads 8i .. 8i+7
+              const float4 wa = wv[2 * i];
+              const float4 wb = wv[2 * i + 1];
+              const float r0 = fmaxf(__uint_as_float(x[8 * i + 0]), 0.f);
+              const float r1 = fmaxf(__uint_as_float(x[8 * i + 1]), 0.f);
+              const float r2 = fmaxf(__uint_as_float(x[8 * i + 2]), 0.f);
+              const float r3 = fmaxf(__uint_as_float(x[8 * i + 3]), 0.f);
+              const float r4 = fmaxf(__uint_as_float(x[8 * i + 4]), 0.f);
+              const float r5 = fmaxf(__uint_as_float(x[8 * i + 5]), 0.f);
+              const float r6 = fmaxf(__uint_as_float(x[8 * i + 6]), 0.f);
+              const float r7 = fmaxf(__uint_as_float(x[8 * i + 7]), 0.f);
+              ffma2(ps[0], ps[1], wa.x, wa.y, r0, r1);
+              ffma2(ps[2], ps[3], wa.z, wa.w, r2, r3);
+              ffma2(ps[4], ps[5], wb.x, wb.y, r4, r5);
+              ffma2(ps[6], ps[7], wb.z, wb.w, r6, r7);
+            }
+            const float score =
+                (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]))) + 0.0f;
+            key32[jj] = ord_key(score);
           }
         }
+        // the accumulator buffer is read: hand it back to the MMA
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.ae(ab));
-        gsync(c);
-        // make room when the next tile could overflow a buffer
-#pragma unroll 1
+        gsync(c);  // (B) the raised thresholds are visible; no append of this tile yet
+#pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * c.g + jj;
-          if (j >= unit.y) continue;
-          const uint32_t n = s_cnt[j];
-          if (n > static_cast<uint32_t>(kCap - kBlockKeys)) {
-            const unsigned long long t =
-                group_compact(c, cand_base + static_cast<size_t>(j) * kCap, n, p.top_k, &s_pos[c.g]);
-            if (c.gtid == 0) {
-              s_cnt[j] = static_cast<uint32_t>(p.top_k);
-              s_thr[j] = t;
+          const int j = 2 * g + jj;
+          if (j < unit.y) {
+            uint32_t* qs = s_qs + j * 4;
+            const bool vis = jl <= unit.w + j;
+            const bool ins = vis && (key32[jj] >> kBinShift) >= qs[2];
+            const uint32_t slot_i = warp_append_slot(ins, &qs[0], lane);
+            if (ins) {
+              st_hint_u64(cand + static_cast<size_t>(j) * kCap + slot_i,
+                          (static_cast<unsigned long long>(key32[jj]) << 32) | static_cast<uint32_t>(unit.z + jl),
+                          pol_cand);
+              hist16_inc(hist_g + jj * (kBins / 2), key32[jj] >> kBinShift);
             }
-            gsync(c);
           }
         }
       }
       if (failed) break;
+      gsync(c);  // every append of the unit is done
+      if (c.gtid < 2) s_fin[slot * kQB + 2 * g + c.gtid] = (2 * g + c.gtid < unit.y) ? s_qs[(2 * g + c.gtid) * 4] : 0u;
+      gsync(c);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bars.ff(slot));
+        mbar_arrive(bars.ue(slot));
+      }
+      ++it;
+    }
+  } else {
+    // ---------------------------------------------------------------- selection group
+    GroupCtx c;
+    c.gwarp = warp - kFirstSelWarp;
+    c.lane = lane;
+    c.gtid = c.gwarp * 32 + lane;
+    c.bar = 3;
+    c.radix = reinterpret_cast<uint32_t*>(smem + kOffRadix) + 256 * 2;
+    c.sel = reinterpret_cast<uint32_t*>(smem + kOffSel) + 8 * 2;
+    uint32_t* ge = reinterpret_cast<uint32_t*>(smem + kOffSelBins);
+    uint32_t* sub = reinterpret_cast<uint32_t*>(smem + kOffSelSub);
+    unsigned long long* stage = reinterpret_cast<unsigned long long*>(smem + kOffStage);
+    uint32_t it = 0;
+    while (true) {
+      const int slot = it & 1;
+      if (!mbar_wait(bars.uf(slot), (it >> 1) & 1, s_abort)) {
+        record_timeout(p, s_abort, 11);
+        atomicOr(&s_gfail[2], 1u);
+      }
+      gsync(c);
+      if (s_gfail[2]) break;
+      const int4 unit = s_unit[slot];
+      if (unit.x < 0) break;
+      if (!mbar_wait(bars.ff(slot), (it >> 1) & 1, s_abort)) {
+        record_timeout(p, s_abort, 12);
+        atomicOr(&s_gfail[2], 1u);
+      }
+      gsync(c);
+      if (s_gfail[2]) break;
+      const unsigned long long* cand = p.cand + (static_cast<size_t>(blockIdx.x) * 2 + slot) * kQB * kCap;
 #pragma unroll 1
-      for (int jj = 0; jj < 2; ++jj) {
-        const int j = 2 * c.g + jj;
-        if (j >= unit.y) continue;
+      for (int j = 0; j < unit.y; ++j) {
         const size_t row = static_cast<size_t>(unit.x + j);
-        group_finish(c, cand_base + static_cast<size_t>(j) * kCap, s_cnt[j], static_cast<uint32_t>(p.top_k), sbuf,
-                     &s_pos[c.g], p.out_ids + row * p.top_k, p.out_scores + row * p.top_k);
+        sel_finish(c, cand + static_cast<size_t>(j) * kCap, s_fin[slot * kQB + j], static_cast<uint32_t>(p.top_k),
+                   ge, sub, stage, s_flags, p.out_ids + row * p.top_k, p.out_scores + row * p.top_k);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars.ue(slot));
+      if (lane == 0) {
+        mbar_arrive(bars.fe(slot));
+        mbar_arrive(bars.ue(slot));
+      }
       ++it;
     }
   }
