@@ -82,6 +82,8 @@ def load():
         "indexer_topk_last_error": (ctypes.c_char_p, []),
         "indexer_topk_version": (ctypes.c_char_p, []),
         "indexer_topk_debug_inject": (ctypes.c_int, [vp, ctypes.c_int, vp]),
+        "indexer_topk_run_noalloc": (ctypes.c_int, [DP, vp, vp, vp, vp, vp, vp]),
+        "indexer_topk_noalloc_scratch_bytes": (sz, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -203,6 +205,16 @@ def indexer_topk_unit_table(desc: Desc):
     if m < 0:
         _check(-m)
     return out[:n]
+
+
+def indexer_topk_run_noalloc(desc: Desc, q, k, w, out_ids, out_scores, stream=None):
+    """The scan through the entry point that allocates nothing (static device scratch).
+
+    For callers that must not allocate device memory at call time, e.g. a runtime that has
+    already reserved the device memory for its own pool. Calls share one scratch array, so
+    calls that overlap on the GPU race; keep them on one stream or ordered."""
+    _check(load().indexer_topk_run_noalloc(desc.ref(), _ptr(q), _ptr(k), _ptr(w), _ptr(out_ids), _ptr(out_scores),
+                                           _stream_handle(stream)))
 
 
 def indexer_topk_debug_inject(plan: Plan, what: int, stream=None):

@@ -454,3 +454,83 @@ int indexer_topk_debug_inject(itk_plan plan, int what, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-allocation entry
+// For callers that cannot allocate device memory at call time: a serving runtime or a
+// framework that has already reserved the device's memory for its own pool (a
+// cudaMalloc would fail or fight that pool), or a latency-critical path where an
+// allocation -- which can synchronize the device -- is not acceptable. The scan's
+// scratch (candidate buffers, unit table, ticket block, status word) lives in this
+// file-scope device array instead of a plan block and a caller workspace. Every GPU that
+// loads this library holds the array until the process exits.
+namespace {
+
+constexpr int kNoAllocMaxCtas = 152;          // CTAs whose candidate buffers fit
+constexpr int64_t kNoAllocMaxUnits = 65536;   // work units (4 queries each) the unit table holds
+constexpr size_t kNoAllocCandBytes = static_cast<size_t>(kNoAllocMaxCtas) * itk::candidate_bytes_per_cta();
+constexpr size_t kNoAllocUnitsOff = kNoAllocCandBytes;
+constexpr size_t kNoAllocTicketOff = kNoAllocUnitsOff + kNoAllocMaxUnits * sizeof(UnitDesc);
+constexpr size_t kNoAllocStatusOff = kNoAllocTicketOff + 256;
+constexpr size_t kNoAllocBytes = kNoAllocStatusOff + 256;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once per device
+// (the host-side symbol is only a stand-in and must never reach a kernel).
+int noalloc_scratch(int device, unsigned char** out) {
+  if (device < 0 || device >= kNoAllocMaxDevices)
+    return fail(ITK_ERR_NO_DEVICE, "device ordinal %d out of range", device);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[device]) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static scratch");
+    g_noalloc_ptr[device] = ptr;
+  }
+  *out = static_cast<unsigned char*>(g_noalloc_ptr[device]);
+  return ITK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t indexer_topk_noalloc_scratch_bytes(void) { return kNoAllocBytes; }
+
+int indexer_topk_run_noalloc(const itk_desc* desc, const void* q, const void* k, const float* w, int32_t* out_ids,
+                             float* out_scores, void* stream) {
+  Layout L;
+  int rc = build_layout(desc, &L);
+  if (rc) return rc;
+  if (L.T == 0) return ITK_OK;
+  if (static_cast<int64_t>(L.units.size()) > kNoAllocMaxUnits)
+    return fail(ITK_ERR_UNSUPPORTED, "%zu work units exceed the static scratch limit of %lld (about %lld queries)",
+                L.units.size(), static_cast<long long>(kNoAllocMaxUnits),
+                static_cast<long long>(kNoAllocMaxUnits) * itk::kQB);
+  DeviceInfo dev;
+  rc = query_device(&dev);
+  if (rc) return rc;
+  rc = check_run_buffers(L, q, k, w, out_ids, out_scores);
+  if (rc) return rc;
+  unsigned char* scratch = nullptr;
+  rc = noalloc_scratch(dev.device, &scratch);
+  if (rc) return rc;
+  const int grid = std::min(grid_for(L.units.size(), dev.sm_count), kNoAllocMaxCtas);
+  // Unit table, then the ticket block and status word, which must start at zero: one copy
+  // on the call's stream (the array keeps the previous call's contents otherwise).
+  const size_t unit_bytes = L.units.size() * sizeof(UnitDesc);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(scratch + kNoAllocUnitsOff, L.units.data(), unit_bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(scratch + kNoAllocTicketOff, 0, kNoAllocBytes - kNoAllocTicketOff, s);
+  if (e != cudaSuccess) return cuda_fail(e, "staging the unit table into the static scratch");
+  return launch_scan(L, grid, reinterpret_cast<const UnitDesc*>(scratch + kNoAllocUnitsOff),
+                     reinterpret_cast<TicketBlock*>(scratch + kNoAllocTicketOff),
+                     reinterpret_cast<uint32_t*>(scratch + kNoAllocStatusOff), q, k, w, out_ids, out_scores, scratch,
+                     s, false);
+}
+
+}  // extern "C"

@@ -174,6 +174,32 @@ ITK_API const char* indexer_topk_last_error(void);
 ITK_API const char* indexer_topk_version(void);
 
 /*
+ * Scan without any device allocation: same operation, arguments and output as
+ * indexer_topk_prepare + indexer_topk_run, but every byte of scratch (candidate buffers,
+ * work-unit table, ticket block, status word) lives in one static device array of
+ * indexer_topk_noalloc_scratch_bytes() bytes (about 41 MB) that every GPU loading this
+ * library holds until the process exits. The paper has no counterpart: it exists for
+ * callers that must not call cudaMalloc at call time -- a serving runtime or framework
+ * that has already reserved the device memory for its own pool, or a latency-critical
+ * path where an allocation, which can synchronize the device, is not acceptable.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call. The
+ *     work-unit table is copied from host memory and the ticket block and status word
+ *     are zeroed on `stream` before the scan; the candidate buffers need no clearing.
+ *   - Limits: at most 65536 work units (4 consecutive queries of one segment each, so
+ *     about 262144 queries), and at most 152 CTAs; larger descriptors are rejected with
+ *     ITK_ERR_UNSUPPORTED and a message from indexer_topk_last_error().
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current) -- make that first call before any stream capture.
+ *   - Every call shares the one array and leaves its contents behind: calls that overlap
+ *     on the GPU race with each other. Issue them on one stream, or order them.
+ */
+ITK_API int indexer_topk_run_noalloc(const itk_desc* desc, const void* q, const void* k, const float* w,
+                                     int32_t* out_ids, float* out_scores, void* stream);
+
+/* Size in bytes of the static scratch array used by indexer_topk_run_noalloc. */
+ITK_API size_t indexer_topk_noalloc_scratch_bytes(void);
+
+/*
  * Test hook for the host-side recovery tests; not part of the operation.
  *   what = 1: the next indexer_topk_run's launch is refused by the CUDA runtime (an
  *             oversized shared-memory request; no work reaches the GPU), as after a run
