@@ -71,6 +71,8 @@ constexpr int kBinShift = 21;                // bin = score key >> 21
 constexpr int kBins = 1 << (32 - kBinShift); // 2048 bins
 constexpr int kStageSlack = 256;             // staging slots past top_k
 constexpr int kBigBucket = 32;               // sub-buckets above this size take the full sort
+constexpr int kSyncEvery = 4;                // epilogue group synchronizes every this many tiles
+constexpr uint32_t kCompactAt = kCap - kSyncEvery * kBlockKeys;  // buffer fill that triggers a compaction
 constexpr int kNumWarps = 14;
 constexpr int kNumThreads = kNumWarps * 32;
 constexpr int kEpiWarps = 8;
@@ -107,7 +109,7 @@ static_assert(kOffK % 1024 == 0 && kKStageBytes % 1024 == 0 && kQHalfBytes % 102
               "SW128 tiles need 1 KB alignment");
 static_assert(kOffBar % 8 == 0 && kOffStage % 16 == 0 && kOffW % 16 == 0, "alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kMaxTopK <= kCap - kBlockKeys, "a compaction to top_k must leave room for a tile");
+static_assert(kMaxTopK <= static_cast<int>(kCompactAt), "a compaction to top_k must leave room for the next tiles");
 static_assert(kCap < 65536, "16-bit histogram counters");
 
 struct UnitDesc {
@@ -354,7 +356,7 @@ __device__ __forceinline__ void epi_compact(const GroupCtx& c, unsigned long lon
   }
   gsync(c);
   uint32_t m = *s_pos;
-  if (m > static_cast<uint32_t>(kCap - kBlockKeys)) {
+  if (m > kCompactAt) {
     // Ties crowd the threshold bin: keep exactly the K largest keys.
     unsigned long long v[kPerThread];
     const uint32_t valid = group_load(c, buf, m, v);
@@ -826,28 +828,32 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool failed = false;
       for (int tile = 0; tile < nt; ++tile, ++ac) {
         const int ab = ac & 1;
+        if (tile % kSyncEvery == 0) {
+          // Group sync point (the only barriers inside a unit): every append of the
+          // earlier tiles is done, so counts and histograms are final.
+          gsync(c);
+          if (s_gfail[g]) {  // uniform: read after the barrier
+            failed = true;
+            break;
+          }
+          // warp jj raises query 2g+jj's threshold bin
+          if (tile > 0 && c.gwarp < 2 && 2 * g + c.gwarp < unit.y)
+            warp_raise_threshold(s_qs + (2 * g + c.gwarp) * 4, hist_g + c.gwarp * (kBins / 2), K, lane);
+          gsync(c);
+          // make room for the appends of the next kSyncEvery tiles (uniform decision)
+#pragma unroll 1
+          for (int jj = 0; jj < 2; ++jj) {
+            const int j = 2 * g + jj;
+            if (j < unit.y && s_qs[j * 4] > kCompactAt)
+              epi_compact(c, cand + static_cast<size_t>(j) * kCap, s_qs + j * 4, hist_g + jj * (kBins / 2), K,
+                          &s_pos[g], pol_cand);
+          }
+        }
         if (!mbar_wait(bars.af(ab), (ac >> 1) & 1, s_abort)) {
           record_timeout(p, s_abort, 10);
-          atomicOr(&s_gfail[g], 1u);
+          atomicOr(&s_gfail[g], 1u);  // the group leaves at its next sync point
+          continue;
         }
-        gsync(c);  // (A) also: every append of the previous tile is done
-        if (s_gfail[g]) {
-          failed = true;
-          break;
-        }
-        // make room when this tile's appends could overflow a buffer (uniform decision;
-        // uses the threshold of the last raise)
-#pragma unroll 1
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * g + jj;
-          if (j < unit.y && s_qs[j * 4] > static_cast<uint32_t>(kCap - kBlockKeys))
-            epi_compact(c, cand + static_cast<size_t>(j) * kCap, s_qs + j * 4, hist_g + jj * (kBins / 2), K,
-                        &s_pos[g], pol_cand);
-        }
-        // warp jj raises query 2g+jj's threshold from the counts of the tiles so far,
-        // while the scores of this tile are computed
-        if (c.gwarp < 2 && 2 * g + c.gwarp < unit.y)
-          warp_raise_threshold(s_qs + (2 * g + c.gwarp) * 4, hist_g + c.gwarp * (kBins / 2), K, lane);
         tc_fence_after_sync();
         const int jl = tile * kBlockKeys + key_lane;  // local key index within the segment
         uint32_t key32[2] = {0u, 0u};
@@ -890,7 +896,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.ae(ab));
-        gsync(c);  // (B) the raised thresholds are visible; no append of this tile yet
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
           const int j = 2 * g + jj;
