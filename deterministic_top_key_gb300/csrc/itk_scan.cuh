@@ -397,6 +397,12 @@ __device__ __forceinline__ void warp_raise_threshold(uint32_t* qs, const uint32_
   uint32_t ge = qs[3] + (n - qs[1]);
   uint32_t thr = qs[2];
   if (ge >= K) {
+    // fast skip over empty runs of 64 bins (one packed word per lane, conflict-free)
+    while ((thr & 1u) == 0 && thr + 64 < static_cast<uint32_t>(kBins)) {
+      const uint32_t word = hist[(thr >> 1) + static_cast<uint32_t>(lane)];
+      if (__any_sync(0xFFFFFFFFu, word != 0u)) break;
+      thr += 64;
+    }
     while (true) {
       const uint32_t b = thr + static_cast<uint32_t>(lane);
       const uint32_t h = b < static_cast<uint32_t>(kBins) ? hist16_get(hist, b) : 0u;
@@ -896,20 +902,28 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.ae(ab));
+        // appends: both queries' slot reservations are issued before either is used
+        bool ins[2];
+        uint32_t m[2], base[2] = {0u, 0u};
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
           const int j = 2 * g + jj;
-          if (j < unit.y) {
-            uint32_t* qs = s_qs + j * 4;
-            const bool vis = jl <= unit.w + j;
-            const bool ins = vis && (key32[jj] >> kBinShift) >= qs[2];
-            const uint32_t slot_i = warp_append_slot(ins, &qs[0], lane);
-            if (ins) {
-              st_hint_u64(cand + static_cast<size_t>(j) * kCap + slot_i,
-                          (static_cast<unsigned long long>(key32[jj]) << 32) | static_cast<uint32_t>(unit.z + jl),
-                          pol_cand);
-              hist16_inc(hist_g + jj * (kBins / 2), key32[jj] >> kBinShift);
-            }
+          ins[jj] = j < unit.y && jl <= unit.w + j && (key32[jj] >> kBinShift) >= s_qs[j * 4 + 2];
+          m[jj] = __ballot_sync(0xFFFFFFFFu, ins[jj]);
+        }
+        const int lead0 = __ffs(m[0]) - 1, lead1 = __ffs(m[1]) - 1;
+        if (m[0] && lane == lead0) base[0] = atomicAdd(&s_qs[(2 * g) * 4], static_cast<uint32_t>(__popc(m[0])));
+        if (m[1] && lane == lead1) base[1] = atomicAdd(&s_qs[(2 * g + 1) * 4], static_cast<uint32_t>(__popc(m[1])));
+        if (m[0]) base[0] = __shfl_sync(0xFFFFFFFFu, base[0], lead0);
+        if (m[1]) base[1] = __shfl_sync(0xFFFFFFFFu, base[1], lead1);
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          if (ins[jj]) {
+            const int j = 2 * g + jj;
+            st_hint_u64(cand + static_cast<size_t>(j) * kCap + base[jj] + __popc(m[jj] & ((1u << lane) - 1u)),
+                        (static_cast<unsigned long long>(key32[jj]) << 32) | static_cast<uint32_t>(unit.z + jl),
+                        pol_cand);
+            hist16_inc(hist_g + jj * (kBins / 2), key32[jj] >> kBinShift);
           }
         }
       }
