@@ -65,14 +65,15 @@ constexpr int kBlockKeys = 128;              // keys per tile (MMA M)
 constexpr int kN = kQB * kHeads;             // MMA N = 256 (query, head) columns
 constexpr int kStages = 3;                   // K tile ring depth
 constexpr int kMaxTopK = 2048;
-constexpr int kCap = 4096;                   // candidate buffer entries per query
+constexpr int kCap = 4096;                   // candidates handed to the selection group per query
+constexpr int kQCap = 8192;                  // candidate buffer entries per query while a unit runs
 constexpr int kPerThread = kCap / 128;       // entries a 128-thread group holds per thread
 constexpr int kBinShift = 21;                // bin = score key >> 21
 constexpr int kBins = 1 << (32 - kBinShift); // 2048 bins
 constexpr int kStageSlack = 256;             // staging slots past top_k
 constexpr int kBigBucket = 32;               // sub-buckets above this size take the full sort
-constexpr int kSyncEvery = 4;                // epilogue group synchronizes every this many tiles
-constexpr uint32_t kCompactAt = kCap - kSyncEvery * kBlockKeys;  // buffer fill that triggers a compaction
+constexpr int kSyncEvery = 8;                // epilogue group synchronizes every this many tiles
+constexpr uint32_t kCompactAt = kQCap - kSyncEvery * kBlockKeys;  // buffer fill that triggers a compaction
 constexpr int kNumWarps = 14;
 constexpr int kNumThreads = kNumWarps * 32;
 constexpr int kEpiWarps = 8;
@@ -110,7 +111,7 @@ static_assert(kOffK % 1024 == 0 && kKStageBytes % 1024 == 0 && kQHalfBytes % 102
 static_assert(kOffBar % 8 == 0 && kOffStage % 16 == 0 && kOffW % 16 == 0, "alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kMaxTopK <= static_cast<int>(kCompactAt), "a compaction to top_k must leave room for the next tiles");
-static_assert(kCap < 65536, "16-bit histogram counters");
+static_assert(kQCap < 65536, "16-bit histogram counters");
 
 struct UnitDesc {
   int32_t q_row0;    // first query row of the unit
@@ -133,13 +134,13 @@ struct ScanParams {
   const float* w;                // [T,64]
   int32_t* out_ids;              // [T,top_k]
   float* out_scores;             // [T,top_k]
-  unsigned long long* cand;      // workspace: gridDim.x x 2 x 4 x kCap candidate keys
+  unsigned long long* cand;      // workspace: per CTA 2 x 4 x kQCap candidate keys, then 2 x kMaxTopK scratch
 };
 
-// Candidate workspace bytes per CTA (two unit buffers of four queries).
-__host__ __device__ constexpr size_t candidate_bytes_per_cta() {
-  return static_cast<size_t>(2) * kQB * kCap * sizeof(unsigned long long);
-}
+// Candidate workspace per CTA: two unit buffers of four queries, then one exact-compaction
+// scratch of kMaxTopK keys per epilogue group.
+constexpr size_t kCandKeysPerCta = static_cast<size_t>(2) * kQB * kQCap + 2 * kMaxTopK;
+__host__ __device__ constexpr size_t candidate_bytes_per_cta() { return kCandKeysPerCta * sizeof(unsigned long long); }
 
 constexpr uint32_t kStatusTimeout = 10u;  // matches ITK_ERR_DEVICE_TIMEOUT
 
@@ -326,13 +327,86 @@ __device__ __forceinline__ uint32_t group_exclusive_scan(const GroupCtx& c, uint
   return total;
 }
 
-// Epilogue-side compaction of one candidate buffer, used when the next tile could
-// overflow it. First drops the keys below the threshold bin (a streaming pass); if that
-// frees too little (many keys in the threshold bin), keeps exactly the K largest keys and
-// rebuilds the histogram from them. Updates the query state (count, threshold bin, keys
-// at or above it) and the histogram.
-__device__ __forceinline__ void epi_compact(const GroupCtx& c, unsigned long long* buf, uint32_t* qs, uint32_t* hist, uint32_t K,
-                            uint32_t* s_pos, uint64_t pol) {
+// Keeps exactly the K largest of the n keys in buf (n > K, any n): a radix select that
+// streams the keys from global memory one byte per pass, then the K keys go through
+// `scratch` back to buf[0..K). Rebuilds the histogram from them and returns the kept
+// keys' lowest bin. Used only when ties crowd one histogram bin, so speed matters little.
+__device__ __noinline__ uint32_t group_exact_stream(const GroupCtx& c, unsigned long long* buf, uint32_t n,
+                                                    uint32_t* hist, uint32_t K, uint32_t* s_cursor,
+                                                    unsigned long long* scratch) {
+  unsigned long long prefix = 0ull;
+  uint32_t k_rem = K;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = c.gtid; i < 256; i += 128) c.radix[i] = 0u;
+    gsync(c);
+    const unsigned long long hi_mask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
+    for (uint32_t i = c.gtid; i < n; i += 128) {
+      const unsigned long long x = buf[i];
+      if ((x & hi_mask) == (prefix & hi_mask)) atomicAdd(&c.radix[(x >> shift) & 0xFFu], 1u);
+    }
+    gsync(c);
+    if (c.gwarp == 0) {
+      uint32_t cnt[8];
+      uint32_t s = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cnt[i] = c.radix[255 - 8 * c.lane - i];
+        s += cnt[i];
+      }
+      uint32_t incl = s;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (c.lane >= off) incl += t;
+      }
+      const uint32_t excl = incl - s;
+      if (excl < k_rem && k_rem <= incl) {
+        uint32_t above = excl;
+        for (int i = 0; i < 8; ++i) {
+          if (above < k_rem && k_rem <= above + cnt[i]) {
+            c.sel[0] = static_cast<uint32_t>(255 - 8 * c.lane - i);
+            c.sel[1] = k_rem - above;
+            c.sel[2] = cnt[i];
+          }
+          above += cnt[i];
+        }
+      }
+    }
+    gsync(c);
+    prefix |= static_cast<unsigned long long>(c.sel[0]) << shift;
+    k_rem = c.sel[1];
+    const uint32_t bucket = c.sel[2];
+    gsync(c);
+    if (bucket == k_rem) break;  // uniform across the group
+  }
+  for (int i = c.gtid; i < kBins / 2; i += 128) hist[i] = 0u;
+  if (c.gtid == 0) *s_cursor = 0u;
+  gsync(c);
+  for (uint32_t base = 0; base < n; base += 128) {
+    const uint32_t i = base + c.gtid;
+    const unsigned long long x = i < n ? buf[i] : 0ull;
+    const bool keep = i < n && x >= prefix;
+    const uint32_t slot = warp_append_slot(keep, s_cursor, c.lane);
+    if (keep) scratch[slot] = x;
+  }
+  gsync(c);
+  for (uint32_t i = c.gtid; i < K; i += 128) {
+    const unsigned long long x = scratch[i];
+    buf[i] = x;
+    hist16_inc(hist, bin_of(x));
+  }
+  gsync(c);
+  return bin_of(prefix);
+}
+
+// Epilogue-side compaction of one candidate buffer, so that at most `limit` keys remain:
+// first drops the keys below the threshold bin (a streaming pass over the group); if more
+// than `limit` keys remain (ties crowd the threshold bin), keeps exactly the K largest and
+// rebuilds the histogram from them. Updates the query state qs: [0] count, [1] count at
+// the last raise, [2] threshold bin, [3] keys at or above the threshold bin.
+__device__ __forceinline__ void epi_compact(const GroupCtx& c, unsigned long long* buf, uint32_t* qs, uint32_t* hist,
+                                            uint32_t K, uint32_t* s_pos, uint64_t pol, uint32_t limit,
+                                            unsigned long long* scratch) {
   constexpr int kChunk = 16;  // keys per thread per pass
   const uint32_t n = qs[0];
   const uint32_t thr = qs[2];
@@ -356,29 +430,11 @@ __device__ __forceinline__ void epi_compact(const GroupCtx& c, unsigned long lon
   }
   gsync(c);
   uint32_t m = *s_pos;
-  if (m > kCompactAt) {
-    // Ties crowd the threshold bin: keep exactly the K largest keys.
-    unsigned long long v[kPerThread];
-    const uint32_t valid = group_load(c, buf, m, v);
-    const unsigned long long prefix = group_select(c, v, valid, K);
-    for (int i = c.gtid; i < kBins / 2; i += 128) hist[i] = 0u;
-    if (c.gtid == 0) *s_pos = 0u;
-    gsync(c);
-#pragma unroll
-    for (int r = 0; r < kPerThread; ++r) {
-      const bool keep = ((valid >> r) & 1u) && v[r] >= prefix;
-      const uint32_t slot = warp_append_slot(keep, s_pos, c.lane);
-      if (keep) {
-        st_hint_u64(buf + slot, v[r], pol);
-        hist16_inc(hist, bin_of(v[r]));
-      }
-    }
-    gsync(c);
+  gsync(c);
+  if (m > limit) {
+    const uint32_t t = group_exact_stream(c, buf, m, hist, K, s_pos, scratch);
     m = K;
-    if (c.gtid == 0) {
-      qs[2] = bin_of(prefix);
-      qs[3] = K;
-    }
+    if (c.gtid == 0) qs[2] = t;
   }
   if (c.gtid == 0) {
     qs[0] = m;
@@ -822,7 +878,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       if (s_gfail[g]) break;
       const int4 unit = s_unit[slot];
       if (unit.x < 0) break;
-      unsigned long long* cand = p.cand + (static_cast<size_t>(blockIdx.x) * 2 + slot) * kQB * kCap;
+      unsigned long long* cand = p.cand + static_cast<size_t>(blockIdx.x) * kCandKeysPerCta + slot * kQB * kQCap;
+      unsigned long long* exact_scratch =
+          p.cand + static_cast<size_t>(blockIdx.x) * kCandKeysPerCta + 2 * kQB * kQCap + g * kMaxTopK;
       for (int i = c.gtid; i < 2 * kHeads; i += 128) {
         const int j = 2 * g + i / kHeads, h = i % kHeads;
         s_w[j * kHeads + h] = j < unit.y ? p.w[static_cast<size_t>(unit.x + j) * kHeads + h] : 0.f;
@@ -851,8 +909,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           for (int jj = 0; jj < 2; ++jj) {
             const int j = 2 * g + jj;
             if (j < unit.y && s_qs[j * 4] > kCompactAt)
-              epi_compact(c, cand + static_cast<size_t>(j) * kCap, s_qs + j * 4, hist_g + jj * (kBins / 2), K,
-                          &s_pos[g], pol_cand);
+              epi_compact(c, cand + static_cast<size_t>(j) * kQCap, s_qs + j * 4, hist_g + jj * (kBins / 2), K,
+                          &s_pos[g], pol_cand, kCompactAt, exact_scratch);
           }
         }
         if (!mbar_wait(bars.af(ab), (ac >> 1) & 1, s_abort)) {
@@ -920,7 +978,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         for (int jj = 0; jj < 2; ++jj) {
           if (ins[jj]) {
             const int j = 2 * g + jj;
-            st_hint_u64(cand + static_cast<size_t>(j) * kCap + base[jj] + __popc(m[jj] & ((1u << lane) - 1u)),
+            st_hint_u64(cand + static_cast<size_t>(j) * kQCap + base[jj] + __popc(m[jj] & ((1u << lane) - 1u)),
                         (static_cast<unsigned long long>(key32[jj]) << 32) | static_cast<uint32_t>(unit.z + jl),
                         pol_cand);
             hist16_inc(hist_g + jj * (kBins / 2), key32[jj] >> kBinShift);
@@ -928,7 +986,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
       }
       if (failed) break;
+      // Hand-off: at most kCap candidates per query go to the selection group.
       gsync(c);  // every append of the unit is done
+      if (c.gwarp < 2 && 2 * g + c.gwarp < unit.y)
+        warp_raise_threshold(s_qs + (2 * g + c.gwarp) * 4, hist_g + c.gwarp * (kBins / 2), K, lane);
+      gsync(c);
+#pragma unroll 1
+      for (int jj = 0; jj < 2; ++jj) {
+        const int j = 2 * g + jj;
+        if (j < unit.y && s_qs[j * 4] > static_cast<uint32_t>(kCap))  // uniform
+          epi_compact(c, cand + static_cast<size_t>(j) * kQCap, s_qs + j * 4, hist_g + jj * (kBins / 2), K,
+                      &s_pos[g], pol_cand, kCap, exact_scratch);
+      }
       if (c.gtid < 2) s_fin[slot * kQB + 2 * g + c.gtid] = (2 * g + c.gtid < unit.y) ? s_qs[(2 * g + c.gtid) * 4] : 0u;
       gsync(c);
       __syncwarp();
@@ -967,11 +1036,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       }
       gsync(c);
       if (s_gfail[2]) break;
-      const unsigned long long* cand = p.cand + (static_cast<size_t>(blockIdx.x) * 2 + slot) * kQB * kCap;
+      const unsigned long long* cand = p.cand + static_cast<size_t>(blockIdx.x) * kCandKeysPerCta + slot * kQB * kQCap;
 #pragma unroll 1
       for (int j = 0; j < unit.y; ++j) {
         const size_t row = static_cast<size_t>(unit.x + j);
-        sel_finish(c, cand + static_cast<size_t>(j) * kCap, s_fin[slot * kQB + j], static_cast<uint32_t>(p.top_k),
+        sel_finish(c, cand + static_cast<size_t>(j) * kQCap, s_fin[slot * kQB + j], static_cast<uint32_t>(p.top_k),
                    ge, sub, stage, s_flags, p.out_ids + row * p.top_k, p.out_scores + row * p.top_k);
       }
       __syncwarp();

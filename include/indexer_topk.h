@@ -177,7 +177,7 @@ ITK_API const char* indexer_topk_version(void);
  * Scan without any device allocation: same operation, arguments and output as
  * indexer_topk_prepare + indexer_topk_run, but every byte of scratch (candidate buffers,
  * work-unit table, ticket block, status word) lives in one static device array of
- * indexer_topk_noalloc_scratch_bytes() bytes (about 41 MB) that every GPU loading this
+ * indexer_topk_noalloc_scratch_bytes() bytes (about 86 MB) that every GPU loading this
  * library holds until the process exits. The paper has no counterpart: it exists for
  * callers that must not call cudaMalloc at call time -- a serving runtime or framework
  * that has already reserved the device memory for its own pool, or a latency-critical
