@@ -158,6 +158,22 @@ def cpu_oracle_sample(wl, budget_s: float, seed_rows: int = 32):
         n = min(wl.T, int(n * max(2.0, budget_s / 3 / max(dt, 1e-3))))
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest value of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank runs its own replica, timed by the slowest rank."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def dist_init():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -297,12 +313,8 @@ def run_ours(args):
     wall = time.perf_counter() - wall0
     plan.device_status()
     per_step_ms = np.array([s.elapsed_time(e) for s, e in zip(starts, ends)])
-    ms = float(per_step_ms.mean())
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * flops / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(float(per_step_ms.mean()), dist, dev)
+    value = job_tflops(flops, world, ms)
 
     # end to end through the public API with pinned host buffers
     e2e = None
@@ -327,14 +339,10 @@ def run_ours(args):
             if i >= args.warmup:
                 e_e[i - args.warmup].record(stream)
         torch.cuda.synchronize()
-        e2e_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(e_s, e_e)]))
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(e_s, e_e)])), dist, dev)
         h2d = hq.numel() * 2 + hk.numel() * 2 + hw.numel() * 4
         d2h = hid.numel() * 4 + hsc.numel() * 4
-        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+        e2e = {"value": job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     # per-config figures (same method; parity-test configs, reported for the roofline)
