@@ -85,25 +85,38 @@ def load_traffic():
 class ClockSampler:
     """nvidia-smi clock/throttle samples taken while the timed region runs."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.timed = None  # (t0, t1) host wall clock of the timed region
 
     def __enter__(self):
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
-                                         stderr=subprocess.DEVNULL)
+                                          "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return self
+        # wait (bounded) for the first sample so that sampling is live before any timed work
+        t_end = time.time() + 10.0
+        while time.time() < t_end and self.proc.poll() is None:
+            self.fh.flush()
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
         return self
+
+    def mark_timed(self, t0: float, t1: float):
+        self.timed = (t0, t1)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -114,28 +127,50 @@ class ClockSampler:
                 self.proc.kill()
             self.fh.close()
 
-    def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons = [], [], set()
+    def _samples(self):
+        import datetime
+
+        out = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    sm, smax = float(parts[2]), float(parts[3])
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
-        if not sm:
+                reasons = {n for n, v in zip(names, parts[6:10]) if v.lower().startswith("active")}
+                out.append((ts, sm, smax, reasons))
+        return out
+
+    def summary(self):
+        """Median SM clock of the samples taken inside the timed region; when that region is
+        shorter than the sampling period, of all samples taken while this benchmark kept the
+        GPU busy (warm-up, timed steps, end-to-end and per-config runs), as `window` says."""
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        samples = self._samples()
+        window = "timed region"
+        if self.timed is not None:
+            # 100 ms of slack: a sample's timestamp is when nvidia-smi started its query
+            inside = [x for x in samples if self.timed[0] - 0.1 <= x[0] <= self.timed[1] + 0.1]
+            if inside:
+                samples_used = inside
+            else:
+                samples_used = samples
+                window = "all GPU work of this run (timed region shorter than the sampling period)"
+        else:
+            samples_used = samples
+            window = "all GPU work of this run"
+        if not samples_used:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = set().union(*[x[3] for x in samples_used])
+        return {"sm_mhz": float(np.median([x[1] for x in samples_used])),
+                "sm_max_mhz": float(max(x[2] for x in samples_used)), "reasons": sorted(reasons),
+                "samples": len(samples_used), "window": window, "period_ms": self.PERIOD_MS}
 
 
 def cpu_oracle_sample(wl, budget_s: float, seed_rows: int = 32):
@@ -293,6 +328,7 @@ def run_ours(args):
 
     wl = inputs.make(args.config, seed=rank)
     flops = 2.0 * visible_pairs(wl) * wl.H * wl.D
+    clocks = ClockSampler(local).__enter__()  # sampling covers warm-up through the per-config runs
     plan, bufs, starts, ends, stream = _measure(binding, torch, wl, dev, args.steps, args.warmup, flush_buf)
     q, k, w, ids, sc, ws = bufs
 
@@ -303,13 +339,14 @@ def run_ours(args):
 
     barrier()
     wall0 = time.perf_counter()
-    with ClockSampler(local) as clocks:
-        for i in range(args.steps):
-            flush_buf.fill_(i & 0xFF)
-            starts[i].record(stream)
-            binding.indexer_topk_run(plan, q, k, w, ids, sc, ws, stream)
-            ends[i].record(stream)
-        barrier()
+    t_timed0 = time.time()
+    for i in range(args.steps):
+        flush_buf.fill_(i & 0xFF)
+        starts[i].record(stream)
+        binding.indexer_topk_run(plan, q, k, w, ids, sc, ws, stream)
+        ends[i].record(stream)
+    barrier()
+    clocks.mark_timed(t_timed0, time.time())
     wall = time.perf_counter() - wall0
     plan.device_status()
     per_step_ms = np.array([s.elapsed_time(e) for s, e in zip(starts, ends)])
@@ -366,6 +403,7 @@ def run_ours(args):
         plan2.destroy()
         del b2
 
+    clocks.__exit__(None, None, None)
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
