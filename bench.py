@@ -31,7 +31,7 @@ if ROOT not in sys.path:
 METRIC = "indexer top-k ms/call and effective TFLOP/s (causal MACs) vs BF16 tensor peak"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "scan_kernel_traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "deterministic_top_key_gb300", "csrc", f)
-                  for f in ("itk_scan.cuh", "itk_ptx.cuh", "itk_host.cu")]
+                  for f in ("itk_common.cuh", "itk_scan.cuh", "itk_select.cuh", "itk_ptx.cuh", "itk_host.cu")]
 
 
 def kernel_source_hash() -> str:

@@ -10,7 +10,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libdtk_indexer_topk.so")
 SOURCES = [os.path.join(CSRC, "itk_host.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("itk_scan.cuh", "itk_ptx.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("itk_common.cuh", "itk_scan.cuh", "itk_select.cuh", "itk_ptx.cuh")] + [
     os.path.join(ROOT, "include", "indexer_topk.h")]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17", "-shared",

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/indexer_topk.h: descriptor validation,
-// work-unit planning, the plan's device block (unit table + ticket block + status word),
-// tensor-map encoding and the single kernel launch per run.
+// work-unit planning, the plan's device block (unit table + two ticket blocks + status
+// word), workspace layout, tensor-map encoding and the two kernel launches per run (the
+// scan, then the selection).
 //
 // Prepared runner and eager entry: flashinfer PR #8691, commit notes "prepare now
 // decides ... before it issues its first device operation", "zero_region ... ABI
@@ -19,6 +20,7 @@
 
 #include "../../include/indexer_topk.h"
 #include "itk_scan.cuh"
+#include "itk_select.cuh"
 
 namespace {
 
@@ -165,26 +167,42 @@ int encode_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_
   return ITK_OK;
 }
 
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int grid_for(size_t n_units, int sm_count) {
   return static_cast<int>(std::min<size_t>(n_units, static_cast<size_t>(sm_count)));
 }
 
-size_t candidate_bytes(int grid) { return static_cast<size_t>(grid) * itk::candidate_bytes_per_cta(); }
-
-// Device block layout shared by the plan and the eager entry: [units | ticket | status].
+// Device block layout shared by the plan and the eager entry:
+// [units | scan ticket | selection ticket | status].
 struct BlockLayout {
-  size_t units_off = 0, ticket_off = 0, status_off = 0, bytes = 0;
+  size_t units_off = 0, ticket_off = 0, sel_ticket_off = 0, status_off = 0, bytes = 0;
 };
 BlockLayout block_layout(size_t n_units) {
   BlockLayout b;
   b.units_off = 0;
   b.ticket_off = align_up(n_units * sizeof(UnitDesc), 64);
-  b.status_off = b.ticket_off + sizeof(TicketBlock);
+  b.sel_ticket_off = b.ticket_off + sizeof(TicketBlock);
+  b.status_off = b.sel_ticket_off + sizeof(TicketBlock);
   b.bytes = b.status_off + 16;
   return b;
 }
+
+// Workspace layout of one run: per-CTA working buffers of the scan, then the candidate
+// store (kCap keys per query slot, four slots per unit), then the per-slot counts.
+struct WorkLayout {
+  size_t cand_off = 0, store_off = 0, counts_off = 0, bytes = 0;
+};
+constexpr WorkLayout work_layout(int grid, size_t n_units) {
+  WorkLayout w;
+  w.cand_off = 0;
+  w.store_off = align_up(static_cast<size_t>(grid) * itk::candidate_bytes_per_cta(), 256);
+  w.counts_off = w.store_off + align_up(n_units * itk::store_bytes_per_unit(), 256);
+  w.bytes = w.counts_off + align_up(n_units * itk::kQB * sizeof(uint32_t), 256);
+  return w;
+}
+
+constexpr size_t kSelSmemLaunch = itk::kSelSmemBytes + 128;  // slack for 128-byte alignment
 
 int ensure_kernel_attributes() {
   static cudaError_t err = cudaErrorUnknown;
@@ -192,6 +210,9 @@ int ensure_kernel_attributes() {
   std::call_once(once, [] {
     err = cudaFuncSetAttribute(itk::indexer_topk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(itk::kSmemBytes));
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(itk::indexer_topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSelSmemLaunch));
   });
   if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute");
   return ITK_OK;
@@ -208,11 +229,12 @@ int check_run_buffers(const Layout& L, const void* q, const void* k, const float
   return ITK_OK;
 }
 
-// Encode maps and launch the scan. `ticket_dirty` asks for a 16-byte zero of the ticket
-// block on the stream first.
-int launch_scan(const Layout& L, int grid, const UnitDesc* d_units, TicketBlock* d_ticket, uint32_t* d_status,
-                const void* q, const void* k, const float* w, int32_t* ids, float* scores, void* cand,
-                cudaStream_t stream, bool force_launch_failure) {
+// Encode maps and launch the scan over units [0, n_units) of d_units, then the selection
+// of the same units' queries. d_ticket points at two adjacent ticket blocks (scan,
+// selection); `work` is laid out by work_layout(grid, n_units).
+int launch_run(const Layout& L, int grid, int sm_count, const UnitDesc* d_units, size_t n_units, TicketBlock* d_ticket,
+               uint32_t* d_status, const void* q, const void* k, const float* w, int32_t* ids, float* scores,
+               void* work, cudaStream_t stream, bool force_launch_failure) {
   CUtensorMap qmap, kmap;
   int rc = encode_rows(&qmap, q, static_cast<uint64_t>(L.T) * itk::kHeads, itk::kN);
   if (rc) return rc;
@@ -220,22 +242,40 @@ int launch_scan(const Layout& L, int grid, const UnitDesc* d_units, TicketBlock*
   if (rc) return rc;
   rc = ensure_kernel_attributes();
   if (rc) return rc;
+  const WorkLayout wl = work_layout(grid, n_units);
+  char* wb = static_cast<char*>(work);
   itk::ScanParams prm;
   prm.units = d_units;
-  prm.n_units = static_cast<int32_t>(L.units.size());
+  prm.n_units = static_cast<int32_t>(n_units);
   prm.top_k = L.top_k;
   prm.ticket = d_ticket;
   prm.status = d_status;
   prm.w = w;
-  prm.out_ids = ids;
-  prm.out_scores = scores;
-  prm.cand = static_cast<unsigned long long*>(cand);
+  prm.cand = reinterpret_cast<unsigned long long*>(wb + wl.cand_off);
+  prm.store = reinterpret_cast<unsigned long long*>(wb + wl.store_off);
+  prm.counts = reinterpret_cast<uint32_t*>(wb + wl.counts_off);
   // A test hook asks for a launch the runtime must refuse: a dynamic shared-memory request
   // above the device limit is rejected at launch time and no work reaches the GPU.
   const size_t smem = force_launch_failure ? size_t(1) << 30 : itk::kSmemBytes;
   itk::indexer_topk_scan_kernel<<<grid, itk::kNumThreads, smem, stream>>>(qmap, kmap, prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "scan launch");
+  itk::SelectParams sp;
+  sp.units = d_units;
+  sp.n_units = static_cast<int32_t>(n_units);
+  sp.top_k = L.top_k;
+  sp.ticket = d_ticket + 1;
+  sp.status = d_status;
+  sp.store = prm.store;
+  sp.counts = prm.counts;
+  sp.out_ids = ids;
+  sp.out_scores = scores;
+  const size_t items = n_units * itk::kQB;
+  const int sel_grid = static_cast<int>(
+      std::max<size_t>(1, std::min<size_t>(static_cast<size_t>(sm_count), (items + itk::kSelGroups - 1) / itk::kSelGroups)));
+  itk::indexer_topk_select_kernel<<<sel_grid, itk::kSelThreads, kSelSmemLaunch, stream>>>(sp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "selection launch");
   return ITK_OK;
 }
 
@@ -270,6 +310,7 @@ const char* indexer_topk_status_string(int status) {
     case ITK_ERR_CUDA: return "CUDA error";
     case ITK_ERR_NO_DEVICE: return "no supported CUDA device";
     case ITK_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case ITK_ERR_INTERNAL: return "internal device check failed";
     default: return "unknown status";
   }
 }
@@ -340,7 +381,7 @@ int indexer_topk_prepare(const itk_desc* desc, void* stream, itk_plan* out_plan)
 
 size_t indexer_topk_workspace_bytes(itk_plan plan) {
   if (!plan) return 0;
-  return plan->grid > 0 ? candidate_bytes(plan->grid) : 0;
+  return plan->grid > 0 ? work_layout(plan->grid, plan->layout.units.size()).bytes : 0;
 }
 
 int indexer_topk_run(itk_plan plan, const void* q, const void* k, const float* w, int32_t* out_ids,
@@ -358,14 +399,14 @@ int indexer_topk_run(itk_plan plan, const void* q, const void* k, const float* w
   char* blk = static_cast<char*>(plan->block);
   TicketBlock* ticket = reinterpret_cast<TicketBlock*>(blk + plan->bl.ticket_off);
   if (plan->ticket_dirty) {
-    cudaError_t e = cudaMemsetAsync(ticket, 0, sizeof(TicketBlock), s);
-    if (e != cudaSuccess) return cuda_fail(e, "zeroing the ticket block");
+    cudaError_t e = cudaMemsetAsync(ticket, 0, 2 * sizeof(TicketBlock), s);
+    if (e != cudaSuccess) return cuda_fail(e, "zeroing the ticket blocks");
   }
   const bool inject = plan->fail_next_launch;
   plan->fail_next_launch = false;
-  rc = launch_scan(L, plan->grid, reinterpret_cast<const UnitDesc*>(blk + plan->bl.units_off), ticket,
-                   reinterpret_cast<uint32_t*>(blk + plan->bl.status_off), q, k, w, out_ids, out_scores, workspace, s,
-                   inject);
+  rc = launch_run(L, plan->grid, plan->dev.sm_count, reinterpret_cast<const UnitDesc*>(blk + plan->bl.units_off),
+                  L.units.size(), ticket, reinterpret_cast<uint32_t*>(blk + plan->bl.status_off), q, k, w, out_ids,
+                  out_scores, workspace, s, inject);
   plan->ticket_dirty = (rc != ITK_OK);
   return rc;
 }
@@ -376,7 +417,7 @@ size_t indexer_topk_eager_workspace_bytes(const itk_desc* desc) {
   DeviceInfo dev;
   if (query_device(&dev)) return 0;
   const int grid = grid_for(L.units.size(), dev.sm_count);
-  return align_up(candidate_bytes(grid), 256) + block_layout(L.units.size()).bytes;
+  return work_layout(grid, L.units.size()).bytes + block_layout(L.units.size()).bytes;
 }
 
 int indexer_topk_eager(const itk_desc* desc, const void* q, const void* k, const float* w, int32_t* out_ids,
@@ -391,7 +432,7 @@ int indexer_topk_eager(const itk_desc* desc, const void* q, const void* k, const
   rc = check_run_buffers(L, q, k, w, out_ids, out_scores);
   if (rc) return rc;
   const int grid = grid_for(L.units.size(), dev.sm_count);
-  const size_t cand = align_up(candidate_bytes(grid), 256);
+  const size_t cand = work_layout(grid, L.units.size()).bytes;
   const BlockLayout bl = block_layout(L.units.size());
   if (!workspace) return fail(ITK_ERR_NULL_POINTER, "workspace is NULL");
   if (workspace_bytes < cand + bl.bytes)
@@ -404,10 +445,10 @@ int indexer_topk_eager(const itk_desc* desc, const void* q, const void* k, const
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(blk, host.data(), bl.bytes, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "uploading the eager unit table");
-  return launch_scan(L, grid, reinterpret_cast<const UnitDesc*>(blk + bl.units_off),
-                     reinterpret_cast<TicketBlock*>(blk + bl.ticket_off),
-                     reinterpret_cast<uint32_t*>(blk + bl.status_off), q, k, w, out_ids, out_scores, workspace, s,
-                     false);
+  return launch_run(L, grid, dev.sm_count, reinterpret_cast<const UnitDesc*>(blk + bl.units_off), L.units.size(),
+                    reinterpret_cast<TicketBlock*>(blk + bl.ticket_off),
+                    reinterpret_cast<uint32_t*>(blk + bl.status_off), q, k, w, out_ids, out_scores, workspace, s,
+                    false);
 }
 
 void indexer_topk_destroy(itk_plan plan) {
@@ -427,8 +468,10 @@ int indexer_topk_device_status(itk_plan plan, void* stream) {
   if (word == 0) return ITK_OK;
   e = cudaMemsetAsync(d_status, 0, sizeof word, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  plan->ticket_dirty = true;  // a run that gave up may have left the ticket block nonzero
+  plan->ticket_dirty = true;  // a run that gave up may have left the ticket blocks nonzero
   if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
+  if ((word & 0xFFu) == itk::kStatusInternal)
+    return fail(ITK_ERR_INTERNAL, "device status word 0x%x (check %u failed)", word, (word >> 8) & 0xFFu);
   return fail(ITK_ERR_DEVICE_TIMEOUT, "device status word 0x%x (wait in role %u gave up)", word, (word >> 8) & 0xFFu);
 }
 
@@ -436,8 +479,8 @@ int indexer_topk_device_status(itk_plan plan, void* stream) {
 // Not part of the operation; used by the host-side recovery tests.
 //   what = 1: the next run's launch is refused by the runtime (oversized shared-memory
 //             request), as after a run that raised while launching.
-//   what = 2: write a nonzero value into the plan's ticket block on `stream`, as a scan
-//             that stopped midway would leave it.
+//   what = 2: write a nonzero value into the plan's two ticket blocks on `stream`, as a
+//             run that stopped midway would leave them.
 int indexer_topk_debug_inject(itk_plan plan, int what, void* stream) {
   if (!plan) return fail(ITK_ERR_INVALID_ARGUMENT, "plan is NULL");
   if (what == 1) {
@@ -446,7 +489,7 @@ int indexer_topk_debug_inject(itk_plan plan, int what, void* stream) {
   }
   if (what == 2) {
     TicketBlock* t = reinterpret_cast<TicketBlock*>(static_cast<char*>(plan->block) + plan->bl.ticket_off);
-    cudaError_t e = cudaMemsetAsync(t, 0x11, sizeof(TicketBlock), static_cast<cudaStream_t>(stream));
+    cudaError_t e = cudaMemsetAsync(t, 0x11, 2 * sizeof(TicketBlock), static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ITK_OK : cuda_fail(e, "poisoning the ticket block");
   }
@@ -459,16 +502,19 @@ int indexer_topk_debug_inject(itk_plan plan, int what, void* stream) {
 // For callers that cannot allocate device memory at call time: a serving runtime or a
 // framework that has already reserved the device's memory for its own pool (a
 // cudaMalloc would fail or fight that pool), or a latency-critical path where an
-// allocation -- which can synchronize the device -- is not acceptable. The scan's
-// scratch (candidate buffers, unit table, ticket block, status word) lives in this
-// file-scope device array instead of a plan block and a caller workspace. Every GPU that
-// loads this library holds the array until the process exits.
+// allocation -- which can synchronize the device -- is not acceptable. The run's scratch
+// (working buffers, candidate store, unit table, ticket blocks, status word) lives in
+// this file-scope device array instead of a plan block and a caller workspace. The
+// candidate store holds kNoAllocChunkUnits work units, so larger inputs run as several
+// scan + selection launch pairs over consecutive ranges of the unit table. Every GPU
+// that loads this library holds the array until the process exits.
 namespace {
 
-constexpr int kNoAllocMaxCtas = 152;          // CTAs whose candidate buffers fit
+constexpr int kNoAllocMaxCtas = 152;          // CTAs whose working buffers fit
+constexpr size_t kNoAllocChunkUnits = 512;    // work units per launch pair (2048 queries)
 constexpr int64_t kNoAllocMaxUnits = 65536;   // work units (4 queries each) the unit table holds
-constexpr size_t kNoAllocCandBytes = static_cast<size_t>(kNoAllocMaxCtas) * itk::candidate_bytes_per_cta();
-constexpr size_t kNoAllocUnitsOff = kNoAllocCandBytes;
+constexpr size_t kNoAllocWorkBytes = work_layout(kNoAllocMaxCtas, kNoAllocChunkUnits).bytes;
+constexpr size_t kNoAllocUnitsOff = kNoAllocWorkBytes;
 constexpr size_t kNoAllocTicketOff = kNoAllocUnitsOff + kNoAllocMaxUnits * sizeof(UnitDesc);
 constexpr size_t kNoAllocStatusOff = kNoAllocTicketOff + 256;
 constexpr size_t kNoAllocBytes = kNoAllocStatusOff + 256;
@@ -519,18 +565,26 @@ int indexer_topk_run_noalloc(const itk_desc* desc, const void* q, const void* k,
   unsigned char* scratch = nullptr;
   rc = noalloc_scratch(dev.device, &scratch);
   if (rc) return rc;
-  const int grid = std::min(grid_for(L.units.size(), dev.sm_count), kNoAllocMaxCtas);
-  // Unit table, then the ticket block and status word, which must start at zero: one copy
-  // on the call's stream (the array keeps the previous call's contents otherwise).
+  // Unit table, then the ticket blocks and status word, which must start at zero: one
+  // copy and one memset on the call's stream (the array keeps the previous call's
+  // contents otherwise). Working buffers, store and counts need no clearing.
   const size_t unit_bytes = L.units.size() * sizeof(UnitDesc);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(scratch + kNoAllocUnitsOff, L.units.data(), unit_bytes, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(scratch + kNoAllocTicketOff, 0, kNoAllocBytes - kNoAllocTicketOff, s);
   if (e != cudaSuccess) return cuda_fail(e, "staging the unit table into the static scratch");
-  return launch_scan(L, grid, reinterpret_cast<const UnitDesc*>(scratch + kNoAllocUnitsOff),
-                     reinterpret_cast<TicketBlock*>(scratch + kNoAllocTicketOff),
-                     reinterpret_cast<uint32_t*>(scratch + kNoAllocStatusOff), q, k, w, out_ids, out_scores, scratch,
-                     s, false);
+  const UnitDesc* d_units = reinterpret_cast<const UnitDesc*>(scratch + kNoAllocUnitsOff);
+  for (size_t u0 = 0; u0 < L.units.size(); u0 += kNoAllocChunkUnits) {
+    const size_t n = std::min(kNoAllocChunkUnits, L.units.size() - u0);
+    // work_layout(grid, n) of a chunk fits inside work_layout(kNoAllocMaxCtas, kNoAllocChunkUnits)
+    const int grid = std::min(grid_for(n, dev.sm_count), kNoAllocMaxCtas);
+    rc = launch_run(L, grid, std::min(dev.sm_count, kNoAllocMaxCtas), d_units + u0, n,
+                    reinterpret_cast<TicketBlock*>(scratch + kNoAllocTicketOff),
+                    reinterpret_cast<uint32_t*>(scratch + kNoAllocStatusOff), q, k, w, out_ids, out_scores,
+                    scratch, s, false);
+    if (rc) return rc;
+  }
+  return ITK_OK;
 }
 
 }  // extern "C"

@@ -1,7 +1,9 @@
 // The scan kernel: persistent CTAs draw work units from a self-resetting ticket word;
 // each unit (up to 4 consecutive queries of one segment) streams its visible key tiles
-// through a tcgen05 GEMM with the keys as the M side, a fused ReLU * w head reduction, a
-// streaming candidate filter, and an exact top-k selection and sort.
+// through a tcgen05 GEMM with the keys as the M side, a fused ReLU * w head reduction and
+// a streaming candidate filter. At the end of a unit each query's candidates (a superset
+// of its top-k, at most kCap keys) go to the query's slot of the candidate store, where
+// the selection kernel picks and sorts the top-k.
 //
 // Operation: flashinfer PR #8691 ("perf(cake_dsa_indexer_det): ticket scheduling on
 // sm_107a, no fill kernel in eager entry"), opening description -- BF16 q/k, FP32 w and
@@ -12,16 +14,14 @@
 // (each running CTA takes the next unit, so a CTA that cannot start does not hold back a
 // second wave) and the TicketWord note (every completed scan leaves the word at zero).
 //
-// CTA layout (448 threads, one CTA per SM):
+// CTA layout (320 threads, one CTA per SM):
 //   warp 0        ticket draws, TMA loads of the Q block and of the K tile ring
 //   warp 1        TMEM allocation, tcgen05.mma issue (one thread)
 //   warps 2..9    epilogue: two groups of four warps; group g owns queries 2g, 2g+1 of
 //                 the unit; the four warps of a group cover the 128 TMEM lanes (keys).
 //                 Per key tile: scores, candidate filter, appends to the query's
-//                 candidate buffer, histogram of the appended score keys.
-//   warps 10..13  selection group: after a unit's last tile, exact top-k of each query's
-//                 candidates, sort, output rows -- while the other warps already run the
-//                 next unit (candidate buffers and their counts are double-buffered).
+//                 working buffer, histogram of the appended score keys; at the end of
+//                 the unit, the hand-off to the candidate store.
 //
 // Score arithmetic (fixed, so a score depends only on q[t], k[s] and w[t], never on
 // tiling, unit or CTA): the tensor core forms the FP32 dot products x_h = q[t,h,:].k[s,:]
@@ -29,57 +29,30 @@
 // s keeps eight partial sums p_m (m = 0..7), p_m = fma(w[t,h], max(x_h, 0), p_m) over
 // h = m, m+8, ..., m+56 in that order, and returns
 //     ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7)) + 0
-// (the "+ 0" turns a -0 into +0). Selection compares (score, id) pairs packed into one
-// 64-bit key (order-preserving score bits above the id bits), so the order is total and
-// the selected set and its order are unique.
+// (the "+ 0" turns a -0 into +0).
 //
-// Candidate filter: a query's candidate buffer holds keys whose score key lies in a bin
+// Candidate filter: a query's working buffer holds keys whose score key lies in a bin
 // (top 11 bits of the order-preserving score key) at or above a threshold bin; the
 // threshold bin is the highest bin whose bins-at-or-above hold at least top_k appended
 // keys. It only rises, and every key it rejects is below top_k keys already seen, so the
 // buffer always contains the exact top-k of the keys seen so far. Every count of that
 // histogram is at most the buffer capacity (keys of bins below the threshold are never
 // appended again), so 16-bit counters, two to a word, suffice.
-//
-// Final selection and sort (selection group): the candidates are counted into the same
-// 2048 bins; the bins that reach the first top_k positions are kept, and each kept bin
-// b with c_b keys is spread over c_b sub-buckets by linear position inside the bin, so
-// sub-buckets hold about one key each. Counting, a prefix sum and a scatter put every
-// key into its sub-bucket's slot range, in descending order of sub-bucket; sorting each
-// (tiny) sub-bucket in place finishes the order. Two exact fallbacks handle heavy ties: a
-// radix select inside an oversized sub-bucket that crosses position top_k, and a full
-// bitonic sort when some sub-bucket is large.
 #pragma once
 
-#include <cuda.h>
-#include <cstdint>
-
-#include "itk_ptx.cuh"
+#include "itk_common.cuh"
 
 namespace itk {
 
-constexpr int kHeads = 64;
-constexpr int kDim = 128;
-constexpr int kQB = 4;                       // queries per work unit
-constexpr int kBlockKeys = 128;              // keys per tile (MMA M)
 constexpr int kN = kQB * kHeads;             // MMA N = 256 (query, head) columns
 constexpr int kStages = 3;                   // K tile ring depth
-constexpr int kMaxTopK = 2048;
-constexpr int kCap = 4096;                   // candidates handed to the selection group per query
-constexpr int kQCap = 8192;                  // candidate buffer entries per query while a unit runs
-constexpr int kPerThread = kCap / 128;       // entries a 128-thread group holds per thread
-constexpr int kBinShift = 21;                // bin = score key >> 21
-constexpr int kBins = 1 << (32 - kBinShift); // 2048 bins
-constexpr int kStageSlack = 256;             // staging slots past top_k
-constexpr int kBigBucket = 32;               // sub-buckets above this size take the full sort
-constexpr int kSyncEvery = 8;                // epilogue group synchronizes every this many tiles
+constexpr int kQCap = 16384;                 // working buffer entries per query while a unit runs
+constexpr int kSyncEvery = 16;               // epilogue group synchronizes every this many tiles
 constexpr uint32_t kCompactAt = kQCap - kSyncEvery * kBlockKeys;  // buffer fill that triggers a compaction
-constexpr int kNumWarps = 14;
+constexpr int kNumWarps = 10;
 constexpr int kNumThreads = kNumWarps * 32;
 constexpr int kEpiWarps = 8;
-constexpr int kSelWarps = 4;
 constexpr int kFirstEpiWarp = 2;
-constexpr int kFirstSelWarp = 10;
 constexpr uint32_t kTmemCols = 512;          // two accumulator buffers of 256 columns
 
 constexpr uint32_t kQHalfBytes = kN * 64 * 2;           // 256 rows x 128 B = 32 KB
@@ -91,39 +64,23 @@ constexpr uint32_t kKStageBytes = 2 * kKHalfBytes;       // 32 KB
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
 constexpr uint32_t kOffHist = kOffK + kStages * kKStageBytes;          // 4 queries x 1024 words (2 x u16 bins)
-constexpr uint32_t kOffSelBins = kOffHist + kQB * (kBins / 2) * 4;     // 2048 x u32
-constexpr uint32_t kOffSelSub = kOffSelBins + kBins * 4;               // 4096 x u32
-constexpr uint32_t kOffStage = kOffSelSub + kCap * 4;                  // (2048 + 256) x u64
-constexpr uint32_t kOffW = kOffStage + (kMaxTopK + kStageSlack) * 8;   // 4 queries x 64 floats
-constexpr uint32_t kOffRadix = kOffW + kQB * kHeads * 4;               // 3 groups x 256 x u32
-constexpr uint32_t kOffQState = kOffRadix + 3 * 256 * 4;               // 4 queries x 4 x u32
-constexpr uint32_t kOffFinCnt = kOffQState + kQB * 16;                 // 2 buffers x 4 x u32
-constexpr uint32_t kOffSel = kOffFinCnt + 2 * kQB * 4;                 // 3 groups x 8 x u32
-constexpr uint32_t kOffUnit = kOffSel + 3 * 8 * 4;                     // 2 slots x int4
-constexpr uint32_t kOffBar = kOffUnit + 2 * 16;                        // mbarriers
-constexpr uint32_t kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 2 + 1;
+constexpr uint32_t kOffW = kOffHist + kQB * (kBins / 2) * 4;           // 4 queries x 64 floats
+constexpr uint32_t kOffRadix = kOffW + kQB * kHeads * 4;               // 2 groups x 256 x u32
+constexpr uint32_t kOffQState = kOffRadix + 2 * 256 * 4;               // 4 queries x 4 x u32
+constexpr uint32_t kOffSel = kOffQState + kQB * 16;                    // 2 groups x 8 x u32
+constexpr uint32_t kOffUnit = kOffSel + 2 * 8 * 4;                     // 2 slots x (int4 unit, int unit index)
+constexpr uint32_t kOffBar = kOffUnit + 2 * 32;                        // mbarriers
+constexpr uint32_t kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;                  // tmem base, abort, flags
 constexpr uint32_t kSmemUsed = kOffMisc + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;                      // slack for 1024-byte alignment
 
 static_assert(kOffK % 1024 == 0 && kKStageBytes % 1024 == 0 && kQHalfBytes % 1024 == 0,
               "SW128 tiles need 1 KB alignment");
-static_assert(kOffBar % 8 == 0 && kOffStage % 16 == 0 && kOffW % 16 == 0, "alignment");
+static_assert(kOffBar % 8 == 0 && kOffW % 16 == 0 && kOffUnit % 16 == 0, "alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kMaxTopK <= static_cast<int>(kCompactAt), "a compaction to top_k must leave room for the next tiles");
 static_assert(kQCap < 65536, "16-bit histogram counters");
-
-struct UnitDesc {
-  int32_t q_row0;    // first query row of the unit
-  int32_t nq;        // queries in the unit (1..4)
-  int32_t key_row0;  // first key row of the unit's segment
-  int32_t pos0;      // causal position of the first query within its segment
-};
-
-struct TicketBlock {
-  unsigned long long next;  // next unit to hand out
-  unsigned long long done;  // CTAs that finished drawing
-};
 
 struct ScanParams {
   const UnitDesc* units;
@@ -132,49 +89,30 @@ struct ScanParams {
   TicketBlock* ticket;
   uint32_t* status;              // device status word (0 = ok)
   const float* w;                // [T,64]
-  int32_t* out_ids;              // [T,top_k]
-  float* out_scores;             // [T,top_k]
-  unsigned long long* cand;      // workspace: per CTA 2 x 4 x kQCap candidate keys, then 2 x kMaxTopK scratch
+  unsigned long long* cand;      // per CTA: 4 x kQCap working keys, then 2 x kMaxTopK exact-select scratch
+  unsigned long long* store;     // [n_units * 4][kCap] candidate keys handed to the selection kernel
+  uint32_t* counts;              // [n_units * 4] keys in each store slot
 };
 
-// Candidate workspace per CTA: two unit buffers of four queries, then one exact-compaction
-// scratch of kMaxTopK keys per epilogue group.
-constexpr size_t kCandKeysPerCta = static_cast<size_t>(2) * kQB * kQCap + 2 * kMaxTopK;
+constexpr size_t kCandKeysPerCta = static_cast<size_t>(kQB) * kQCap + 2 * kMaxTopK;
 __host__ __device__ constexpr size_t candidate_bytes_per_cta() { return kCandKeysPerCta * sizeof(unsigned long long); }
-
-constexpr uint32_t kStatusTimeout = 10u;  // matches ITK_ERR_DEVICE_TIMEOUT
-
-__device__ __forceinline__ uint32_t ord_key(float f) {
-  const uint32_t b = __float_as_uint(f);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float key_to_float(uint32_t o) {
-  const uint32_t b = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
-  return __uint_as_float(b);
-}
-__device__ __forceinline__ uint32_t bin_of(unsigned long long key) {
-  return static_cast<uint32_t>(key >> (32 + kBinShift));
+// Candidate store bytes per work unit (four query slots of kCap keys, then the counts live apart).
+__host__ __device__ constexpr size_t store_bytes_per_unit() {
+  return static_cast<size_t>(kQB) * kCap * sizeof(unsigned long long);
 }
 
 struct Bars {
-  uint32_t kfull, kempty, qfull, qempty, accfull, accempty, unitfull, unitempty, finfull, finempty, mmadone;
+  uint32_t kfull, kempty, qfull, qempty, accfull, accempty, unitfull, unitempty, mmadone;
   __device__ uint32_t kf(int s) const { return kfull + 8u * s; }
   __device__ uint32_t ke(int s) const { return kempty + 8u * s; }
   __device__ uint32_t af(int b) const { return accfull + 8u * b; }
   __device__ uint32_t ae(int b) const { return accempty + 8u * b; }
   __device__ uint32_t uf(int s) const { return unitfull + 8u * s; }
   __device__ uint32_t ue(int s) const { return unitempty + 8u * s; }
-  __device__ uint32_t ff(int b) const { return finfull + 8u * b; }
-  __device__ uint32_t fe(int b) const { return finempty + 8u * b; }
 };
 
 __device__ __forceinline__ int n_tiles_of(const int4& u) {
   return (u.w + u.y + kBlockKeys - 1) / kBlockKeys;  // ceil((pos0 + nq) / 128)
-}
-
-__device__ __forceinline__ void record_timeout(const ScanParams& p, volatile uint32_t* abort_flag, uint32_t role) {
-  *abort_flag = 1u;
-  atomicOr(p.status, kStatusTimeout | (role << 8));
 }
 
 // Two FP32 fused multiply-adds in one instruction: (d0, d1) = (a0*b0 + d0, a1*b1 + d1),
@@ -196,144 +134,11 @@ __device__ __forceinline__ uint32_t hist16_get(const uint32_t* h, uint32_t b) {
 }
 __device__ __forceinline__ void hist16_inc(uint32_t* h, uint32_t b) { atomicAdd(&h[b >> 1], 1u << ((b & 1u) * 16u)); }
 
-// ------------------------------------------------------------------ 128-thread groups
-struct GroupCtx {
-  int gtid;        // 0..127
-  int gwarp;       // 0..3
-  int lane;
-  uint32_t bar;    // named barrier id
-  uint32_t* radix; // 256 bins of radix-select scratch
-  uint32_t* sel;   // 8 words of scratch
-};
-
-__device__ __forceinline__ void gsync(const GroupCtx& c) { named_bar_sync(c.bar, 128); }
-
-// Warp-aggregated append: lanes with `pred` get consecutive slots from *counter.
-__device__ __forceinline__ uint32_t warp_append_slot(bool pred, uint32_t* counter, int lane) {
-  const uint32_t m = __ballot_sync(0xFFFFFFFFu, pred);
-  uint32_t base = 0;
-  if (m) {
-    const int leader = __ffs(m) - 1;
-    if (lane == leader) base = atomicAdd(counter, static_cast<uint32_t>(__popc(m)));
-    base = __shfl_sync(0xFFFFFFFFu, base, leader);
-  }
-  return base + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
-}
-
-// Radix select over keys held in registers (entry r valid iff bit r of `valid`): returns
-// `prefix` with #{valid x : x >= prefix} == K (1 <= K <= number of valid keys). Digits
-// of 8 bits from the top; stops as soon as the bucket holding the K-th largest key is
-// selected whole.
-__device__ unsigned long long group_select(const GroupCtx& c, const unsigned long long (&v)[kPerThread],
-                                           uint32_t valid, uint32_t K) {
-  unsigned long long prefix = 0ull;
-  uint32_t k_rem = K;
-  for (int shift = 56; shift >= 0; shift -= 8) {
-    for (int i = c.gtid; i < 256; i += 128) c.radix[i] = 0u;
-    gsync(c);
-    const unsigned long long hi_mask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
-#pragma unroll
-    for (int r = 0; r < kPerThread; ++r) {
-      if (((valid >> r) & 1u) && ((v[r] & hi_mask) == (prefix & hi_mask)))
-        atomicAdd(&c.radix[(v[r] >> shift) & 0xFFu], 1u);
-    }
-    gsync(c);
-    if (c.gwarp == 0) {
-      uint32_t cnt[8];
-      uint32_t s = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        cnt[i] = c.radix[255 - 8 * c.lane - i];
-        s += cnt[i];
-      }
-      uint32_t incl = s;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (c.lane >= off) incl += t;
-      }
-      const uint32_t excl = incl - s;
-      if (excl < k_rem && k_rem <= incl) {
-        uint32_t above = excl;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (above < k_rem && k_rem <= above + cnt[i]) {
-            c.sel[0] = static_cast<uint32_t>(255 - 8 * c.lane - i);
-            c.sel[1] = k_rem - above;
-            c.sel[2] = cnt[i];
-          }
-          above += cnt[i];
-        }
-      }
-    }
-    gsync(c);
-    const uint32_t b = c.sel[0];
-    k_rem = c.sel[1];
-    const uint32_t bucket = c.sel[2];
-    prefix |= static_cast<unsigned long long>(b) << shift;
-    if (bucket == k_rem) break;  // uniform across the group
-  }
-  gsync(c);  // c.sel may be reused right after
-  return prefix;
-}
-
-// Loads the first n keys of buf into registers (entry gtid + 128*r); returns the valid mask.
-__device__ __forceinline__ uint32_t group_load(const GroupCtx& c, const unsigned long long* buf, uint32_t n,
-                                               unsigned long long (&v)[kPerThread]) {
-  uint32_t valid = 0;
-#pragma unroll
-  for (int r = 0; r < kPerThread; ++r) {
-    const uint32_t idx = c.gtid + 128u * r;
-    v[r] = idx < n ? buf[idx] : 0ull;
-    valid |= (idx < n ? 1u : 0u) << r;
-  }
-  return valid;
-}
-
-// Exclusive prefix sum of a[0..n) in place (n <= 128 * per), 128 threads; returns the total.
-template <int kPer>
-__device__ __forceinline__ uint32_t group_exclusive_scan(const GroupCtx& c, uint32_t* a, uint32_t n) {
-  uint32_t loc[kPer];
-  uint32_t s = 0;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const uint32_t idx = c.gtid * kPer + i;
-    loc[i] = idx < n ? a[idx] : 0u;
-    s += loc[i];
-  }
-  uint32_t incl = s;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-    if (c.lane >= off) incl += t;
-  }
-  if (c.lane == 31) c.sel[4 + c.gwarp] = incl;
-  gsync(c);
-  uint32_t base = 0, total = 0;
-#pragma unroll
-  for (int wv = 0; wv < 4; ++wv) {
-    const uint32_t x = c.sel[4 + wv];
-    base += wv < c.gwarp ? x : 0u;
-    total += x;
-  }
-  uint32_t run = base + incl - s;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const uint32_t idx = c.gtid * kPer + i;
-    if (idx < n) a[idx] = run;
-    run += loc[i];
-  }
-  gsync(c);
-  return total;
-}
-
-// Keeps exactly the K largest of the n keys in buf (n > K, any n): a radix select that
-// streams the keys from global memory one byte per pass, then the K keys go through
-// `scratch` back to buf[0..K). Rebuilds the histogram from them and returns the kept
-// keys' lowest bin. Used only when ties crowd one histogram bin, so speed matters little.
-__device__ __noinline__ uint32_t group_exact_stream(const GroupCtx& c, unsigned long long* buf, uint32_t n,
-                                                    uint32_t* hist, uint32_t K, uint32_t* s_cursor,
-                                                    unsigned long long* scratch) {
+// Radix select streamed from global memory, one byte per pass: returns `prefix` with
+// #{x in buf[0..n) : x >= prefix} == K (K <= n, keys distinct). Used only when ties crowd
+// one histogram bin, so speed matters little.
+__device__ __noinline__ unsigned long long group_select_stream(const GroupCtx& c, const unsigned long long* buf,
+                                                               uint32_t n, uint32_t K) {
   unsigned long long prefix = 0ull;
   uint32_t k_rem = K;
   for (int shift = 56; shift >= 0; shift -= 8) {
@@ -345,33 +150,7 @@ __device__ __noinline__ uint32_t group_exact_stream(const GroupCtx& c, unsigned 
       if ((x & hi_mask) == (prefix & hi_mask)) atomicAdd(&c.radix[(x >> shift) & 0xFFu], 1u);
     }
     gsync(c);
-    if (c.gwarp == 0) {
-      uint32_t cnt[8];
-      uint32_t s = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        cnt[i] = c.radix[255 - 8 * c.lane - i];
-        s += cnt[i];
-      }
-      uint32_t incl = s;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (c.lane >= off) incl += t;
-      }
-      const uint32_t excl = incl - s;
-      if (excl < k_rem && k_rem <= incl) {
-        uint32_t above = excl;
-        for (int i = 0; i < 8; ++i) {
-          if (above < k_rem && k_rem <= above + cnt[i]) {
-            c.sel[0] = static_cast<uint32_t>(255 - 8 * c.lane - i);
-            c.sel[1] = k_rem - above;
-            c.sel[2] = cnt[i];
-          }
-          above += cnt[i];
-        }
-      }
-    }
+    group_pick_digit(c, k_rem);
     gsync(c);
     prefix |= static_cast<unsigned long long>(c.sel[0]) << shift;
     k_rem = c.sel[1];
@@ -379,7 +158,15 @@ __device__ __noinline__ uint32_t group_exact_stream(const GroupCtx& c, unsigned 
     gsync(c);
     if (bucket == k_rem) break;  // uniform across the group
   }
-  for (int i = c.gtid; i < kBins / 2; i += 128) hist[i] = 0u;
+  return prefix;
+}
+
+// Appends the keys of buf[0..n) at or above `prefix` to dst[0..limit) through the group
+// cursor *s_cursor (reset here); returns the number appended.
+__device__ __forceinline__ uint32_t group_keep_at_or_above(const GroupCtx& c, const unsigned long long* buf,
+                                                           uint32_t n, unsigned long long prefix,
+                                                           unsigned long long* dst, uint32_t limit,
+                                                           uint32_t* s_cursor) {
   if (c.gtid == 0) *s_cursor = 0u;
   gsync(c);
   for (uint32_t base = 0; base < n; base += 128) {
@@ -387,9 +174,21 @@ __device__ __noinline__ uint32_t group_exact_stream(const GroupCtx& c, unsigned 
     const unsigned long long x = i < n ? buf[i] : 0ull;
     const bool keep = i < n && x >= prefix;
     const uint32_t slot = warp_append_slot(keep, s_cursor, c.lane);
-    if (keep) scratch[slot] = x;
+    if (keep && slot < limit) dst[slot] = x;  // exactly `limit` keys qualify: keys are distinct
   }
   gsync(c);
+  const uint32_t m = *s_cursor;
+  gsync(c);
+  return m < limit ? m : limit;
+}
+
+// Keeps exactly the K largest of the n keys in buf (n > K): they go through `scratch`
+// back to buf[0..K), and the histogram is rebuilt from them. Returns their lowest bin.
+__device__ uint32_t group_exact_in_place(const GroupCtx& c, unsigned long long* buf, uint32_t n, uint32_t* hist,
+                                         uint32_t K, uint32_t* s_cursor, unsigned long long* scratch) {
+  const unsigned long long prefix = group_select_stream(c, buf, n, K);
+  for (int i = c.gtid; i < kBins / 2; i += 128) hist[i] = 0u;
+  group_keep_at_or_above(c, buf, n, prefix, scratch, K, s_cursor);
   for (uint32_t i = c.gtid; i < K; i += 128) {
     const unsigned long long x = scratch[i];
     buf[i] = x;
@@ -399,17 +198,13 @@ __device__ __noinline__ uint32_t group_exact_stream(const GroupCtx& c, unsigned 
   return bin_of(prefix);
 }
 
-// Epilogue-side compaction of one candidate buffer, so that at most `limit` keys remain:
-// first drops the keys below the threshold bin (a streaming pass over the group); if more
-// than `limit` keys remain (ties crowd the threshold bin), keeps exactly the K largest and
-// rebuilds the histogram from them. Updates the query state qs: [0] count, [1] count at
-// the last raise, [2] threshold bin, [3] keys at or above the threshold bin.
-__device__ __forceinline__ void epi_compact(const GroupCtx& c, unsigned long long* buf, uint32_t* qs, uint32_t* hist,
-                                            uint32_t K, uint32_t* s_pos, uint64_t pol, uint32_t limit,
-                                            unsigned long long* scratch) {
+// Drops the keys of buf[0..n) whose bin is below thr, writing the survivors to dst[0..limit)
+// (dst may be buf itself: every key of a chunk is read before any slot of it is
+// rewritten); returns the number that qualified (callers make sure it is <= limit).
+__device__ __forceinline__ uint32_t group_drop_below(const GroupCtx& c, unsigned long long* buf, uint32_t n,
+                                                     uint32_t thr, unsigned long long* dst, uint32_t limit,
+                                                     uint32_t* s_pos, uint64_t pol) {
   constexpr int kChunk = 16;  // keys per thread per pass
-  const uint32_t n = qs[0];
-  const uint32_t thr = qs[2];
   if (c.gtid == 0) *s_pos = 0u;
   gsync(c);
   for (uint32_t base = 0; base < n; base += 128 * kChunk) {
@@ -419,20 +214,31 @@ __device__ __forceinline__ void epi_compact(const GroupCtx& c, unsigned long lon
       const uint32_t idx = base + c.gtid + 128u * r;
       x[r] = idx < n ? ld_hint_u64(buf + idx, pol) : 0ull;
     }
-    gsync(c);  // every key of this chunk is read before any slot of it is rewritten
+    gsync(c);
 #pragma unroll
     for (int r = 0; r < kChunk; ++r) {
       const uint32_t idx = base + c.gtid + 128u * r;
       const bool keep = idx < n && bin_of(x[r]) >= thr;
       const uint32_t slot = warp_append_slot(keep, s_pos, c.lane);
-      if (keep) st_hint_u64(buf + slot, x[r], pol);
+      if (keep && slot < limit) st_hint_u64(dst + slot, x[r], pol);
     }
   }
   gsync(c);
-  uint32_t m = *s_pos;
+  const uint32_t m = *s_pos;
   gsync(c);
+  return m;
+}
+
+// Mid-unit compaction of one working buffer, so that at most `limit` keys remain: drops
+// the keys below the threshold bin; if more than `limit` remain (ties crowd the threshold
+// bin), keeps exactly the K largest. Updates the query state qs: [0] count, [1] count at
+// the last raise, [2] threshold bin, [3] keys at or above the threshold bin.
+__device__ __forceinline__ void epi_compact(const GroupCtx& c, unsigned long long* buf, uint32_t* qs, uint32_t* hist,
+                                            uint32_t K, uint32_t* s_pos, uint64_t pol, uint32_t limit,
+                                            unsigned long long* scratch) {
+  uint32_t m = group_drop_below(c, buf, qs[0], qs[2], buf, kQCap, s_pos, pol);
   if (m > limit) {
-    const uint32_t t = group_exact_stream(c, buf, m, hist, K, s_pos, scratch);
+    const uint32_t t = group_exact_in_place(c, buf, m, hist, K, s_pos, scratch);
     m = K;
     if (c.gtid == 0) qs[2] = t;
   }
@@ -442,6 +248,29 @@ __device__ __forceinline__ void epi_compact(const GroupCtx& c, unsigned long lon
     qs[3] = m;  // every kept key lies at or above the threshold bin
   }
   gsync(c);
+}
+
+// End of a unit for one query: its candidates (every key of the working buffer in a bin
+// at or above the threshold, or exactly the K largest when more than kCap of those
+// remain) go to its store slot, and their number to *count.
+__device__ __forceinline__ void epi_handoff(const GroupCtx& c, unsigned long long* buf, const uint32_t* qs, uint32_t K,
+                                            uint32_t* s_pos, uint64_t pol, unsigned long long* dst, uint32_t* count,
+                                            uint32_t* status) {
+  const uint32_t n = qs[0];
+  uint32_t m;
+  if (qs[3] > static_cast<uint32_t>(kCap)) {  // uniform; qs[3] counts the keys at or above the threshold bin
+    const unsigned long long prefix = group_select_stream(c, buf, n, K);
+    m = group_keep_at_or_above(c, buf, n, prefix, dst, K, s_pos);
+  } else {
+    m = group_drop_below(c, buf, n, qs[2], dst, kCap, s_pos, pol);
+  }
+  if (c.gtid == 0) {
+    if (m > static_cast<uint32_t>(kCap)) {  // cannot happen: qs[3] is the exact number kept
+      atomicOr(status, kStatusInternal | (21u << 8));
+      m = kCap;
+    }
+    *count = m;
+  }
 }
 
 // Raise a query's threshold bin as far as its histogram allows, by one warp: afterwards
@@ -485,177 +314,6 @@ __device__ __forceinline__ void warp_raise_threshold(uint32_t* qs, const uint32_
   }
 }
 
-// Bitonic sort (descending) of a[0..np2) in shared memory, np2 a power of two.
-__device__ void group_bitonic_desc(const GroupCtx& c, unsigned long long* a, uint32_t np2) {
-  for (uint32_t size = 2; size <= np2; size <<= 1) {
-    for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
-      for (uint32_t i = c.gtid; i < np2 / 2; i += 128) {
-        const uint32_t lo = 2 * i - (i & (stride - 1));
-        const uint32_t hi = lo + stride;
-        const bool desc = (lo & size) == 0;
-        const unsigned long long x = a[lo], y = a[hi];
-        if ((x < y) == desc) {
-          a[lo] = y;
-          a[hi] = x;
-        }
-      }
-      gsync(c);
-    }
-  }
-}
-
-// Slot-range index (in descending key order) of a kept key. ge[b] counts kept candidates
-// in bins >= b; bin b's keys own sub-buckets [ge[b+1], ge[b]) by linear position inside
-// the bin (higher key first).
-__device__ __forceinline__ uint32_t sub_bucket(const uint32_t* ge, unsigned long long x) {
-  const uint32_t b = bin_of(x);
-  const uint32_t above = b + 1 < static_cast<uint32_t>(kBins) ? ge[b + 1] : 0u;
-  const uint32_t cb = ge[b] - above;
-  const uint32_t frac = static_cast<uint32_t>(x >> 32) & ((1u << kBinShift) - 1u);  // position inside the bin
-  const uint32_t sub = ((frac >> 9) * cb) >> (kBinShift - 9);                       // 0 .. cb-1
-  return above + (cb - 1u - sub);
-}
-
-// Selection group: exact top-k of one query's candidates, sorted by the total order,
-// written as one output row.
-__device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned long long* buf, uint32_t n, uint32_t top_k,
-                           uint32_t* ge, uint32_t* sub, unsigned long long* stage, uint32_t* flags, int32_t* out_ids,
-                           float* out_scores) {
-  unsigned long long v[kPerThread];
-  const uint32_t valid = group_load(c, buf, n, v);
-  const uint32_t keff = n < top_k ? n : top_k;
-  // count the candidates per bin
-  for (int i = c.gtid; i < kBins; i += 128) ge[i] = 0u;
-  if (c.gtid == 0) {
-    flags[0] = kBins - 1;  // first kept bin
-    flags[1] = 0u;         // large sub-bucket seen
-    flags[2] = 0xFFFFFFFFu;  // sub-bucket that crosses top_k and overflows the staging area
-  }
-  gsync(c);
-#pragma unroll
-  for (int r = 0; r < kPerThread; ++r)
-    if ((valid >> r) & 1u) atomicAdd(&ge[bin_of(v[r])], 1u);
-  gsync(c);
-  // ge[b] = candidates in bins >= b (suffix sums, 16 bins per thread, highest bins first)
-  {
-    uint32_t loc[16];
-    uint32_t s = 0;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      loc[i] = ge[kBins - 1 - (16 * c.gtid + i)];
-      s += loc[i];
-    }
-    uint32_t incl = s;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-      if (c.lane >= off) incl += t;
-    }
-    if (c.lane == 31) c.sel[4 + c.gwarp] = incl;
-    gsync(c);
-    uint32_t run = incl - s;
-#pragma unroll
-    for (int wv = 0; wv < 4; ++wv) run += wv < c.gwarp ? c.sel[4 + wv] : 0u;
-    uint32_t first_kept = kBins - 1;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t b = kBins - 1 - (16 * c.gtid + i);
-      // run = candidates in bins above b; bin b reaches a position below top_k iff run < top_k
-      if (run < top_k) first_kept = b;
-      run += loc[i];
-      ge[b] = run;
-    }
-    atomicMin(&flags[0], first_kept);
-  }
-  gsync(c);
-  const uint32_t tstar = flags[0];
-  const uint32_t m_keep = ge[tstar];  // candidates in kept bins
-  for (uint32_t i = c.gtid; i < m_keep; i += 128) sub[i] = 0u;
-  gsync(c);
-  uint32_t kept = 0;  // bit r: candidate r lies in a kept bin
-#pragma unroll
-  for (int r = 0; r < kPerThread; ++r) {
-    if (((valid >> r) & 1u) && bin_of(v[r]) >= tstar) {
-      kept |= 1u << r;
-      atomicAdd(&sub[sub_bucket(ge, v[r])], 1u);
-    }
-  }
-  gsync(c);
-  group_exclusive_scan<kPerThread>(c, sub, m_keep);  // sub[i] = first slot of sub-bucket i
-  const uint32_t cap = top_k + kStageSlack;
-#pragma unroll
-  for (int r = 0; r < kPerThread; ++r) {
-    if ((kept >> r) & 1u) {
-      const uint32_t pos = atomicAdd(&sub[sub_bucket(ge, v[r])], 1u);
-      if (pos < cap) stage[pos] = v[r];
-    }
-  }
-  gsync(c);
-  // sub[i] is now the end of sub-bucket i; sort every sub-bucket that reaches a slot below
-  // top_k, in place (they hold about one key each)
-  for (uint32_t i = c.gtid; i < m_keep; i += 128) {
-    const uint32_t start = i ? sub[i - 1] : 0u;
-    const uint32_t end = sub[i];
-    if (start >= keff || end - start < 2) continue;
-    if (end > keff && (end > cap || end - start > static_cast<uint32_t>(kBigBucket))) {
-      flags[2] = i;  // the one sub-bucket that crosses position keff, too large to sort here
-      continue;
-    }
-    if (end - start > static_cast<uint32_t>(kBigBucket)) {
-      flags[1] = 1u;
-      continue;
-    }
-    for (uint32_t a = start + 1; a < end; ++a) {
-      const unsigned long long x = stage[a];
-      uint32_t b = a;
-      while (b > start && stage[b - 1] < x) {
-        stage[b] = stage[b - 1];
-        --b;
-      }
-      stage[b] = x;
-    }
-  }
-  gsync(c);
-  const uint32_t over = flags[2];
-  if (over != 0xFFFFFFFFu) {
-    // exact fallback: keep the (keff - start) largest keys of the crossing sub-bucket
-    const uint32_t start = over ? sub[over - 1] : 0u;
-    uint32_t in_b = 0;
-#pragma unroll
-    for (int r = 0; r < kPerThread; ++r)
-      if (((kept >> r) & 1u) && sub_bucket(ge, v[r]) == over) in_b |= 1u << r;
-    const unsigned long long pfx = group_select(c, v, in_b, keff - start);
-    if (c.gtid == 0) flags[3] = start;
-    gsync(c);
-#pragma unroll
-    for (int r = 0; r < kPerThread; ++r) {
-      const bool take = ((in_b >> r) & 1u) && v[r] >= pfx;
-      const uint32_t slot = warp_append_slot(take, &flags[3], c.lane);
-      if (take) stage[slot] = v[r];
-    }
-    if (c.gtid == 0) flags[1] = 1u;  // the refilled range is unsorted
-    gsync(c);
-  }
-  if (flags[1]) {
-    uint32_t np2 = 2;
-    while (np2 < keff) np2 <<= 1;
-    for (uint32_t i = keff + c.gtid; i < np2; i += 128) stage[i] = 0ull;
-    gsync(c);
-    group_bitonic_desc(c, stage, np2);
-  }
-  for (uint32_t r = c.gtid; r < top_k; r += 128) {
-    if (r < keff) {
-      const unsigned long long x = stage[r];
-      st_stream_s32(out_ids + r, static_cast<int32_t>(static_cast<uint32_t>(x & 0xFFFFFFFFull)));
-      st_stream_f32(out_scores + r, key_to_float(static_cast<uint32_t>(x >> 32)));
-    } else {
-      st_stream_s32(out_ids + r, -1);
-      st_stream_f32(out_scores + r, -__int_as_float(0x7F800000));
-    }
-  }
-  gsync(c);
-}
-
 // ------------------------------------------------------------------ the kernel
 __global__ void __launch_bounds__(kNumThreads, 1)
     indexer_topk_scan_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
@@ -668,15 +326,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   // per-query epilogue state: [j][0] count, [1] count at the last threshold raise,
   // [2] threshold bin, [3] keys appended at or above the threshold bin
   uint32_t* s_qs = reinterpret_cast<uint32_t*>(smem + kOffQState);
-  uint32_t* s_fin = reinterpret_cast<uint32_t*>(smem + kOffFinCnt);  // [buffer][query] final counts
-  int4* s_unit = reinterpret_cast<int4*>(smem + kOffUnit);
+  int4* s_unit = reinterpret_cast<int4*>(smem + kOffUnit);            // [slot * 2]: unit; [slot * 2 + 1].x: index
   float* s_w = reinterpret_cast<float*>(smem + kOffW);
   uint32_t* s_misc = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   uint32_t* s_tmem = s_misc + 0;
   volatile uint32_t* s_abort = s_misc + 1;
-  uint32_t* s_gfail = s_misc + 2;  // [3] per-group failure flags
+  uint32_t* s_gfail = s_misc + 2;  // [2] per-group failure flags
   uint32_t* s_pos = s_misc + 6;    // [2] epilogue-group cursors
-  uint32_t* s_flags = s_misc + 8;  // [4] selection-group flags
 
   const uint32_t bar0 = smem_u32(smem + kOffBar);
   Bars bars;
@@ -688,9 +344,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   bars.accempty = bars.accfull + 16;
   bars.unitfull = bars.accempty + 16;
   bars.unitempty = bars.unitfull + 16;
-  bars.finfull = bars.unitempty + 16;
-  bars.finempty = bars.finfull + 16;
-  bars.mmadone = bars.finempty + 16;
+  bars.mmadone = bars.unitempty + 16;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -703,9 +357,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bars.af(b), 1);
       mbar_init(bars.ae(b), kEpiWarps);
       mbar_init(bars.uf(b), 1);
-      mbar_init(bars.ue(b), 1 + kEpiWarps + kSelWarps);
-      mbar_init(bars.ff(b), kEpiWarps);
-      mbar_init(bars.fe(b), kSelWarps);
+      mbar_init(bars.ue(b), 1 + kEpiWarps);
     }
     mbar_init(bars.mmadone, 1);
     for (int i = 1; i < 16; ++i) s_misc[i] = 0u;
@@ -735,7 +387,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const unsigned long long u = atomicAdd(&p.ticket->next, 1ull);
         const int slot = it & 1;
         if (!mbar_wait(bars.ue(slot), ((it >> 1) & 1) ^ 1, s_abort)) {
-          record_timeout(p, s_abort, 1);
+          record_timeout(p.status, s_abort, 1);
           break;
         }
         int4 unit;
@@ -745,11 +397,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         } else {
           unit = make_int4(-1, 0, 0, 0);
         }
-        s_unit[slot] = unit;
+        s_unit[2 * slot] = unit;
+        s_unit[2 * slot + 1] = make_int4(static_cast<int>(u), 0, 0, 0);
         mbar_arrive(bars.uf(slot));
         if (unit.x < 0) break;
         if (!mbar_wait(bars.qempty, (it & 1) ^ 1, s_abort)) {
-          record_timeout(p, s_abort, 2);
+          record_timeout(p.status, s_abort, 2);
           break;
         }
         mbar_arrive_expect_tx(bars.qfull, kQBytes);
@@ -761,7 +414,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         for (int tile = 0; tile < nt; ++tile, ++kc) {
           const int s = kc % kStages;
           if (!mbar_wait(bars.ke(s), ((kc / kStages) & 1) ^ 1, s_abort)) {
-            record_timeout(p, s_abort, 3);
+            record_timeout(p.status, s_abort, 3);
             ok = false;
             break;
           }
@@ -778,13 +431,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       for (uint32_t j = (kc > kStages ? kc - kStages : 0); j < kc; ++j)
         mbar_wait(bars.kf(j % kStages), (j / kStages) & 1, nullptr);
       if (qloads > 0) mbar_wait(bars.qfull, (qloads - 1) & 1, nullptr);
-      // The last CTA to finish drawing resets the ticket block for the next scan.
-      __threadfence();
-      const unsigned long long prev = atomicAdd(&p.ticket->done, 1ull);
-      if (prev == static_cast<unsigned long long>(gridDim.x) - 1ull) {
-        atomicExch(&p.ticket->next, 0ull);
-        atomicExch(&p.ticket->done, 0ull);
-      }
+      ticket_release(p.ticket);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
@@ -796,26 +443,26 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       while (ok) {
         const int slot = it & 1;
         if (!mbar_wait(bars.uf(slot), (it >> 1) & 1, s_abort)) {
-          record_timeout(p, s_abort, 4);
+          record_timeout(p.status, s_abort, 4);
           break;
         }
-        const int4 unit = s_unit[slot];
+        const int4 unit = s_unit[2 * slot];
         if (unit.x < 0) break;
         if (!mbar_wait(bars.qfull, it & 1, s_abort)) {
-          record_timeout(p, s_abort, 5);
+          record_timeout(p.status, s_abort, 5);
           break;
         }
         const int nt = n_tiles_of(unit);
         for (int tile = 0; tile < nt; ++tile, ++kc, ++ac) {
           const int ab = ac & 1;
           if (!mbar_wait(bars.ae(ab), ((ac >> 1) & 1) ^ 1, s_abort)) {
-            record_timeout(p, s_abort, 6);
+            record_timeout(p.status, s_abort, 6);
             ok = false;
             break;
           }
           const int s = kc % kStages;
           if (!mbar_wait(bars.kf(s), (kc / kStages) & 1, s_abort)) {
-            record_timeout(p, s_abort, 7);
+            record_timeout(p.status, s_abort, 7);
             ok = false;
             break;
           }
@@ -843,7 +490,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mma_commit(bars.mmadone);
       mbar_wait(bars.mmadone, 0, nullptr);
     }
-  } else if (warp < kFirstSelWarp) {
+  } else {
     // ---------------------------------------------------------------- epilogue
     const int ew = warp - kFirstEpiWarp;
     const int g = ew >> 2;
@@ -860,27 +507,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const uint32_t K = static_cast<uint32_t>(p.top_k);
     const uint64_t pol_cand = policy_evict_last();
     uint32_t* hist_g = reinterpret_cast<uint32_t*>(smem + kOffHist) + (2 * g) * (kBins / 2);
+    unsigned long long* cand = p.cand + static_cast<size_t>(blockIdx.x) * kCandKeysPerCta;
+    unsigned long long* exact_scratch = cand + static_cast<size_t>(kQB) * kQCap + g * kMaxTopK;
 
     uint32_t it = 0, ac = 0;
     while (true) {
-      const int slot = it & 1;  // also the candidate buffer set of this unit
+      const int slot = it & 1;
       // Every decision to leave the loop is taken by the whole group at once (flag set
       // before a group barrier, read after it), so no warp is left waiting at a barrier.
       if (!mbar_wait(bars.uf(slot), (it >> 1) & 1, s_abort)) {
-        record_timeout(p, s_abort, 8);
-        atomicOr(&s_gfail[g], 1u);
-      }
-      if (!mbar_wait(bars.fe(slot), ((it >> 1) & 1) ^ 1, s_abort)) {
-        record_timeout(p, s_abort, 9);
+        record_timeout(p.status, s_abort, 8);
         atomicOr(&s_gfail[g], 1u);
       }
       gsync(c);
       if (s_gfail[g]) break;
-      const int4 unit = s_unit[slot];
+      const int4 unit = s_unit[2 * slot];
       if (unit.x < 0) break;
-      unsigned long long* cand = p.cand + static_cast<size_t>(blockIdx.x) * kCandKeysPerCta + slot * kQB * kQCap;
-      unsigned long long* exact_scratch =
-          p.cand + static_cast<size_t>(blockIdx.x) * kCandKeysPerCta + 2 * kQB * kQCap + g * kMaxTopK;
+      const size_t uidx = static_cast<size_t>(s_unit[2 * slot + 1].x);
       for (int i = c.gtid; i < 2 * kHeads; i += 128) {
         const int j = 2 * g + i / kHeads, h = i % kHeads;
         s_w[j * kHeads + h] = j < unit.y ? p.w[static_cast<size_t>(unit.x + j) * kHeads + h] : 0.f;
@@ -914,7 +557,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
         }
         if (!mbar_wait(bars.af(ab), (ac >> 1) & 1, s_abort)) {
-          record_timeout(p, s_abort, 10);
+          record_timeout(p.status, s_abort, 10);
           atomicOr(&s_gfail[g], 1u);  // the group leaves at its next sync point
           continue;
         }
@@ -925,31 +568,33 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         for (int jj = 0; jj < 2; ++jj) {
           const int j = 2 * g + jj;
           if (j < unit.y) {  // uniform across the group
-            uint32_t x[64];
             const uint32_t col = static_cast<uint32_t>(ab * kN + j * kHeads);
-            tmem_ld32(lane_addr + col, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-            tmem_ld32(lane_addr + col + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
-            tmem_ld_wait();
             const float4* wv = reinterpret_cast<const float4*>(s_w + j * kHeads);
             float ps[8];
 #pragma unroll
             for (int m = 0; m < 8; ++m) ps[m] = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {  // heads 8i .. 8i+7
-              const float4 wa = wv[2 * i];
-              const float4 wb = wv[2 * i + 1];
-              const float r0 = fmaxf(__uint_as_float(x[8 * i + 0]), 0.f);
-              const float r1 = fmaxf(__uint_as_float(x[8 * i + 1]), 0.f);
-              const float r2 = fmaxf(__uint_as_float(x[8 * i + 2]), 0.f);
-              const float r3 = fmaxf(__uint_as_float(x[8 * i + 3]), 0.f);
-              const float r4 = fmaxf(__uint_as_float(x[8 * i + 4]), 0.f);
-              const float r5 = fmaxf(__uint_as_float(x[8 * i + 5]), 0.f);
-              const float r6 = fmaxf(__uint_as_float(x[8 * i + 6]), 0.f);
-              const float r7 = fmaxf(__uint_as_float(x[8 * i + 7]), 0.f);
-              ffma2(ps[0], ps[1], wa.x, wa.y, r0, r1);
-              ffma2(ps[2], ps[3], wa.z, wa.w, r2, r3);
-              ffma2(ps[4], ps[5], wb.x, wb.y, r4, r5);
-              ffma2(ps[6], ps[7], wb.z, wb.w, r6, r7);
+            for (int half = 0; half < 2; ++half) {  // heads 32 half .. 32 half + 31
+              uint32_t x[32];
+              tmem_ld32(lane_addr + col + 32 * half, x);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {  // heads 32 half + 8i .. + 7
+                const float4 wa = wv[8 * half + 2 * i];
+                const float4 wb = wv[8 * half + 2 * i + 1];
+                const float r0 = fmaxf(__uint_as_float(x[8 * i + 0]), 0.f);
+                const float r1 = fmaxf(__uint_as_float(x[8 * i + 1]), 0.f);
+                const float r2 = fmaxf(__uint_as_float(x[8 * i + 2]), 0.f);
+                const float r3 = fmaxf(__uint_as_float(x[8 * i + 3]), 0.f);
+                const float r4 = fmaxf(__uint_as_float(x[8 * i + 4]), 0.f);
+                const float r5 = fmaxf(__uint_as_float(x[8 * i + 5]), 0.f);
+                const float r6 = fmaxf(__uint_as_float(x[8 * i + 6]), 0.f);
+                const float r7 = fmaxf(__uint_as_float(x[8 * i + 7]), 0.f);
+                ffma2(ps[0], ps[1], wa.x, wa.y, r0, r1);
+                ffma2(ps[2], ps[3], wa.z, wa.w, r2, r3);
+                ffma2(ps[4], ps[5], wb.x, wb.y, r4, r5);
+                ffma2(ps[6], ps[7], wb.z, wb.w, r6, r7);
+              }
             }
             const float score =
                 (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]))) + 0.0f;
@@ -986,7 +631,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
       }
       if (failed) break;
-      // Hand-off: at most kCap candidates per query go to the selection group.
+      // Hand-off: every candidate of the unit's queries goes to the store.
       gsync(c);  // every append of the unit is done
       if (c.gwarp < 2 && 2 * g + c.gwarp < unit.y)
         warp_raise_threshold(s_qs + (2 * g + c.gwarp) * 4, hist_g + c.gwarp * (kBins / 2), K, lane);
@@ -994,60 +639,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll 1
       for (int jj = 0; jj < 2; ++jj) {
         const int j = 2 * g + jj;
-        if (j < unit.y && s_qs[j * 4] > static_cast<uint32_t>(kCap))  // uniform
-          epi_compact(c, cand + static_cast<size_t>(j) * kQCap, s_qs + j * 4, hist_g + jj * (kBins / 2), K,
-                      &s_pos[g], pol_cand, kCap, exact_scratch);
+        if (j < unit.y) {  // uniform
+          const size_t item = uidx * kQB + j;
+          epi_handoff(c, cand + static_cast<size_t>(j) * kQCap, s_qs + j * 4, K, &s_pos[g], pol_cand,
+                      p.store + item * kCap, p.counts + item, p.status);
+        }
       }
-      if (c.gtid < 2) s_fin[slot * kQB + 2 * g + c.gtid] = (2 * g + c.gtid < unit.y) ? s_qs[(2 * g + c.gtid) * 4] : 0u;
       gsync(c);
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bars.ff(slot));
-        mbar_arrive(bars.ue(slot));
-      }
-      ++it;
-    }
-  } else {
-    // ---------------------------------------------------------------- selection group
-    GroupCtx c;
-    c.gwarp = warp - kFirstSelWarp;
-    c.lane = lane;
-    c.gtid = c.gwarp * 32 + lane;
-    c.bar = 3;
-    c.radix = reinterpret_cast<uint32_t*>(smem + kOffRadix) + 256 * 2;
-    c.sel = reinterpret_cast<uint32_t*>(smem + kOffSel) + 8 * 2;
-    uint32_t* ge = reinterpret_cast<uint32_t*>(smem + kOffSelBins);
-    uint32_t* sub = reinterpret_cast<uint32_t*>(smem + kOffSelSub);
-    unsigned long long* stage = reinterpret_cast<unsigned long long*>(smem + kOffStage);
-    uint32_t it = 0;
-    while (true) {
-      const int slot = it & 1;
-      if (!mbar_wait(bars.uf(slot), (it >> 1) & 1, s_abort)) {
-        record_timeout(p, s_abort, 11);
-        atomicOr(&s_gfail[2], 1u);
-      }
-      gsync(c);
-      if (s_gfail[2]) break;
-      const int4 unit = s_unit[slot];
-      if (unit.x < 0) break;
-      if (!mbar_wait(bars.ff(slot), (it >> 1) & 1, s_abort)) {
-        record_timeout(p, s_abort, 12);
-        atomicOr(&s_gfail[2], 1u);
-      }
-      gsync(c);
-      if (s_gfail[2]) break;
-      const unsigned long long* cand = p.cand + static_cast<size_t>(blockIdx.x) * kCandKeysPerCta + slot * kQB * kQCap;
-#pragma unroll 1
-      for (int j = 0; j < unit.y; ++j) {
-        const size_t row = static_cast<size_t>(unit.x + j);
-        sel_finish(c, cand + static_cast<size_t>(j) * kQCap, s_fin[slot * kQB + j], static_cast<uint32_t>(p.top_k),
-                   ge, sub, stage, s_flags, p.out_ids + row * p.top_k, p.out_scores + row * p.top_k);
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bars.fe(slot));
-        mbar_arrive(bars.ue(slot));
-      }
+      if (lane == 0) mbar_arrive(bars.ue(slot));
       ++it;
     }
   }

@@ -1,0 +1,307 @@
+// The selection kernel: exact top-k of each query's candidate list (written by the scan
+// kernel), sorted by the total order of the 64-bit selection key, written as the query's
+// output row of ids and scores.
+//
+// Operation: flashinfer PR #8691, opening description -- top-k key ids and scores per
+// query, ties to the larger id; the candidate lists hold every key of the query's top-k
+// (the scan's filter only drops keys below top_k keys already seen), so selecting within
+// them gives the exact answer.
+//
+// Work distribution: a persistent grid; each 128-thread group draws one query at a time
+// from a self-resetting ticket word (same page, commit note on drawing work units from
+// the ticket word and the TicketWord note).
+//
+// Per query (n candidates, keff = min(n, top_k) outputs): the candidates are counted into
+// the 2048 bins of their score's top 11 bits; the bins that reach the first top_k
+// positions are kept, and each kept bin b with c_b keys is spread over c_b sub-buckets by
+// linear position inside the bin, so sub-buckets hold about one key each. Counting, a
+// prefix sum and a scatter put every key into its sub-bucket's slot range, in descending
+// order of sub-bucket; sorting each (tiny) sub-bucket in place finishes the order. Two
+// exact fallbacks handle heavy ties: a radix select inside an oversized sub-bucket that
+// crosses position top_k, and a full bitonic sort when some sub-bucket is large.
+#pragma once
+
+#include "itk_common.cuh"
+
+namespace itk {
+
+constexpr int kSelGroups = 4;                 // 128-thread groups per selection CTA
+constexpr int kSelThreads = kSelGroups * 128;
+constexpr int kStageSlack = 256;              // staging slots past top_k
+constexpr int kBigBucket = 32;                // sub-buckets above this size take the full sort
+
+// Per-group shared memory of the selection kernel (offsets within the group's slice).
+constexpr uint32_t kSgBins = 0;                                        // 2048 x u32
+constexpr uint32_t kSgSub = kSgBins + kBins * 4;                       // 4096 x u32
+constexpr uint32_t kSgStage = kSgSub + kCap * 4;                       // (2048 + 256) x u64
+constexpr uint32_t kSgRadix = kSgStage + (kMaxTopK + kStageSlack) * 8; // 256 x u32
+constexpr uint32_t kSgSel = kSgRadix + 256 * 4;                        // 8 x u32
+constexpr uint32_t kSgFlags = kSgSel + 8 * 4;                          // 4 x u32
+constexpr uint32_t kSgItem = kSgFlags + 4 * 4;                         // 4 x u32 (drawn item)
+constexpr uint32_t kSgBytes = (kSgItem + 16 + 127) / 128 * 128;
+constexpr uint32_t kSelSmemBytes = kSelGroups * kSgBytes;
+static_assert(kSgStage % 16 == 0, "alignment");
+static_assert(kSelSmemBytes <= 232448, "shared memory budget");
+
+struct SelectParams {
+  const UnitDesc* units;              // the scan's unit table; item i is query i % 4 of unit i / 4
+  int32_t n_units;
+  int32_t top_k;
+  TicketBlock* ticket;
+  uint32_t* status;
+  const unsigned long long* store;    // [n_units * 4][kCap] candidate keys
+  const uint32_t* counts;             // [n_units * 4] candidates per item
+  int32_t* out_ids;                   // [T, top_k]
+  float* out_scores;                  // [T, top_k]
+};
+
+// Exclusive prefix sum of a[0..n) in place (n <= 128 * kPer), 128 threads; returns the total.
+template <int kPer>
+__device__ __forceinline__ uint32_t group_exclusive_scan(const GroupCtx& c, uint32_t* a, uint32_t n) {
+  uint32_t loc[kPer];
+  uint32_t s = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const uint32_t idx = c.gtid * kPer + i;
+    loc[i] = idx < n ? a[idx] : 0u;
+    s += loc[i];
+  }
+  uint32_t incl = s;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (c.lane >= off) incl += t;
+  }
+  if (c.lane == 31) c.sel[4 + c.gwarp] = incl;
+  gsync(c);
+  uint32_t base = 0, total = 0;
+#pragma unroll
+  for (int wv = 0; wv < 4; ++wv) {
+    const uint32_t x = c.sel[4 + wv];
+    base += wv < c.gwarp ? x : 0u;
+    total += x;
+  }
+  uint32_t run = base + incl - s;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const uint32_t idx = c.gtid * kPer + i;
+    if (idx < n) a[idx] = run;
+    run += loc[i];
+  }
+  gsync(c);
+  return total;
+}
+
+// Bitonic sort (descending) of a[0..np2) in shared memory, np2 a power of two.
+__device__ void group_bitonic_desc(const GroupCtx& c, unsigned long long* a, uint32_t np2) {
+  for (uint32_t size = 2; size <= np2; size <<= 1) {
+    for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
+      for (uint32_t i = c.gtid; i < np2 / 2; i += 128) {
+        const uint32_t lo = 2 * i - (i & (stride - 1));
+        const uint32_t hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const unsigned long long x = a[lo], y = a[hi];
+        if ((x < y) == desc) {
+          a[lo] = y;
+          a[hi] = x;
+        }
+      }
+      gsync(c);
+    }
+  }
+}
+
+// Slot-range index (in descending key order) of a kept key. ge[b] counts kept candidates
+// in bins >= b; bin b's keys own sub-buckets [ge[b+1], ge[b]) by linear position inside
+// the bin (higher key first).
+__device__ __forceinline__ uint32_t sub_bucket(const uint32_t* ge, unsigned long long x) {
+  const uint32_t b = bin_of(x);
+  const uint32_t above = b + 1 < static_cast<uint32_t>(kBins) ? ge[b + 1] : 0u;
+  const uint32_t cb = ge[b] - above;
+  const uint32_t frac = static_cast<uint32_t>(x >> 32) & ((1u << kBinShift) - 1u);  // position inside the bin
+  const uint32_t sub = ((frac >> 9) * cb) >> (kBinShift - 9);                       // 0 .. cb-1
+  return above + (cb - 1u - sub);
+}
+
+// Exact top-k of one query's n candidates (buf[0..n), n <= kCap), sorted by the total
+// order, written as one output row.
+__device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned long long* buf, uint32_t n,
+                                           uint32_t top_k, uint32_t* ge, uint32_t* sub, unsigned long long* stage,
+                                           uint32_t* flags, int32_t* out_ids, float* out_scores) {
+  unsigned long long v[kPerThread];
+  const uint32_t valid = group_load(c, buf, n, v);
+  const uint32_t keff = n < top_k ? n : top_k;
+  // count the candidates per bin
+  for (int i = c.gtid; i < kBins; i += 128) ge[i] = 0u;
+  if (c.gtid == 0) {
+    flags[0] = kBins - 1;    // first kept bin
+    flags[1] = 0u;           // large sub-bucket seen
+    flags[2] = 0xFFFFFFFFu;  // sub-bucket that crosses top_k and overflows the staging area
+  }
+  gsync(c);
+#pragma unroll
+  for (int r = 0; r < kPerThread; ++r)
+    if ((valid >> r) & 1u) atomicAdd(&ge[bin_of(v[r])], 1u);
+  gsync(c);
+  // ge[b] = candidates in bins >= b (suffix sums, 16 bins per thread, highest bins first)
+  {
+    uint32_t loc[16];
+    uint32_t s = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      loc[i] = ge[kBins - 1 - (16 * c.gtid + i)];
+      s += loc[i];
+    }
+    uint32_t incl = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (c.lane >= off) incl += t;
+    }
+    if (c.lane == 31) c.sel[4 + c.gwarp] = incl;
+    gsync(c);
+    uint32_t run = incl - s;
+#pragma unroll
+    for (int wv = 0; wv < 4; ++wv) run += wv < c.gwarp ? c.sel[4 + wv] : 0u;
+    uint32_t first_kept = kBins - 1;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t b = kBins - 1 - (16 * c.gtid + i);
+      // run = candidates in bins above b; bin b reaches a position below top_k iff run < top_k
+      if (run < top_k) first_kept = b;
+      run += loc[i];
+      ge[b] = run;
+    }
+    atomicMin(&flags[0], first_kept);
+  }
+  gsync(c);
+  const uint32_t tstar = flags[0];
+  const uint32_t m_keep = ge[tstar];  // candidates in kept bins
+  for (uint32_t i = c.gtid; i < m_keep; i += 128) sub[i] = 0u;
+  gsync(c);
+  uint32_t kept = 0;  // bit r: candidate r lies in a kept bin
+#pragma unroll
+  for (int r = 0; r < kPerThread; ++r) {
+    if (((valid >> r) & 1u) && bin_of(v[r]) >= tstar) {
+      kept |= 1u << r;
+      atomicAdd(&sub[sub_bucket(ge, v[r])], 1u);
+    }
+  }
+  gsync(c);
+  group_exclusive_scan<kPerThread>(c, sub, m_keep);  // sub[i] = first slot of sub-bucket i
+  const uint32_t cap = top_k + kStageSlack;
+#pragma unroll
+  for (int r = 0; r < kPerThread; ++r) {
+    if ((kept >> r) & 1u) {
+      const uint32_t pos = atomicAdd(&sub[sub_bucket(ge, v[r])], 1u);
+      if (pos < cap) stage[pos] = v[r];
+    }
+  }
+  gsync(c);
+  // sub[i] is now the end of sub-bucket i; sort every sub-bucket that reaches a slot below
+  // top_k, in place (they hold about one key each)
+  for (uint32_t i = c.gtid; i < m_keep; i += 128) {
+    const uint32_t start = i ? sub[i - 1] : 0u;
+    const uint32_t end = sub[i];
+    if (start >= keff || end - start < 2) continue;
+    if (end > keff && (end > cap || end - start > static_cast<uint32_t>(kBigBucket))) {
+      flags[2] = i;  // the one sub-bucket that crosses position keff, too large to sort here
+      continue;
+    }
+    if (end - start > static_cast<uint32_t>(kBigBucket)) {
+      flags[1] = 1u;
+      continue;
+    }
+    for (uint32_t a = start + 1; a < end; ++a) {
+      const unsigned long long x = stage[a];
+      uint32_t b = a;
+      while (b > start && stage[b - 1] < x) {
+        stage[b] = stage[b - 1];
+        --b;
+      }
+      stage[b] = x;
+    }
+  }
+  gsync(c);
+  const uint32_t over = flags[2];
+  if (over != 0xFFFFFFFFu) {
+    // exact fallback: keep the (keff - start) largest keys of the crossing sub-bucket
+    const uint32_t start = over ? sub[over - 1] : 0u;
+    uint32_t in_b = 0;
+#pragma unroll
+    for (int r = 0; r < kPerThread; ++r)
+      if (((kept >> r) & 1u) && sub_bucket(ge, v[r]) == over) in_b |= 1u << r;
+    const unsigned long long pfx = group_select(c, v, in_b, keff - start);
+    if (c.gtid == 0) flags[3] = start;
+    gsync(c);
+#pragma unroll
+    for (int r = 0; r < kPerThread; ++r) {
+      const bool take = ((in_b >> r) & 1u) && v[r] >= pfx;
+      const uint32_t slot = warp_append_slot(take, &flags[3], c.lane);
+      if (take && slot < keff) stage[slot] = v[r];  // exactly keff - start keys qualify: keys are distinct
+    }
+    if (c.gtid == 0) flags[1] = 1u;  // the refilled range is unsorted
+    gsync(c);
+  }
+  if (flags[1]) {
+    uint32_t np2 = 2;
+    while (np2 < keff) np2 <<= 1;
+    for (uint32_t i = keff + c.gtid; i < np2; i += 128) stage[i] = 0ull;
+    gsync(c);
+    group_bitonic_desc(c, stage, np2);
+  }
+  for (uint32_t r = c.gtid; r < top_k; r += 128) {
+    if (r < keff) {
+      const unsigned long long x = stage[r];
+      st_stream_s32(out_ids + r, static_cast<int32_t>(static_cast<uint32_t>(x & 0xFFFFFFFFull)));
+      st_stream_f32(out_scores + r, key_to_float(static_cast<uint32_t>(x >> 32)));
+    } else {
+      st_stream_s32(out_ids + r, -1);
+      st_stream_f32(out_scores + r, -__int_as_float(0x7F800000));
+    }
+  }
+  gsync(c);
+}
+
+__global__ void __launch_bounds__(kSelThreads, 1) indexer_topk_select_kernel(const SelectParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  const int g = threadIdx.x >> 7;
+  uint8_t* gs = smem + g * kSgBytes;
+  GroupCtx c;
+  c.gtid = threadIdx.x & 127;
+  c.gwarp = c.gtid >> 5;
+  c.lane = threadIdx.x & 31;
+  c.bar = 1 + g;
+  c.radix = reinterpret_cast<uint32_t*>(gs + kSgRadix);
+  c.sel = reinterpret_cast<uint32_t*>(gs + kSgSel);
+  uint32_t* ge = reinterpret_cast<uint32_t*>(gs + kSgBins);
+  uint32_t* sub = reinterpret_cast<uint32_t*>(gs + kSgSub);
+  unsigned long long* stage = reinterpret_cast<unsigned long long*>(gs + kSgStage);
+  uint32_t* flags = reinterpret_cast<uint32_t*>(gs + kSgFlags);
+  volatile unsigned long long* s_item = reinterpret_cast<volatile unsigned long long*>(gs + kSgItem);
+  const unsigned long long n_items = static_cast<unsigned long long>(p.n_units) * kQB;
+
+  while (true) {
+    if (c.gtid == 0) *s_item = atomicAdd(&p.ticket->next, 1ull);
+    gsync(c);
+    const unsigned long long item = *s_item;
+    gsync(c);  // every thread has read the item before the next draw overwrites it
+    if (item >= n_items) break;
+    const UnitDesc u = p.units[item / kQB];
+    const int j = static_cast<int>(item % kQB);
+    if (j >= u.nq) continue;
+    const size_t row = static_cast<size_t>(u.q_row0 + j);
+    uint32_t n = p.counts[item];
+    if (n > static_cast<uint32_t>(kCap)) {  // cannot happen: the scan hands off at most kCap keys
+      if (c.gtid == 0) atomicOr(p.status, kStatusInternal | (20u << 8));
+      n = kCap;
+    }
+    sel_finish(c, p.store + item * kCap, n, static_cast<uint32_t>(p.top_k), ge, sub, stage, flags,
+               p.out_ids + row * p.top_k, p.out_scores + row * p.top_k);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) ticket_release(p.ticket);
+}
+
+}  // namespace itk

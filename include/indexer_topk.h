@@ -70,7 +70,8 @@ enum {
   ITK_ERR_WORKSPACE_TOO_SMALL = 7,/* workspace_bytes below indexer_topk_workspace_bytes() */
   ITK_ERR_CUDA = 8,               /* a CUDA runtime call or the kernel launch failed */
   ITK_ERR_NO_DEVICE = 9,          /* no CUDA device, or the device is not sm_103 */
-  ITK_ERR_DEVICE_TIMEOUT = 10     /* a bounded wait inside the kernel ran out (see indexer_topk_device_status) */
+  ITK_ERR_DEVICE_TIMEOUT = 10,    /* a bounded wait inside the kernel ran out (see indexer_topk_device_status) */
+  ITK_ERR_INTERNAL = 11           /* a kernel found one of its own invariants broken (see indexer_topk_device_status) */
 };
 
 typedef struct itk_plan_s* itk_plan;
@@ -91,8 +92,8 @@ typedef struct {
 /*
  * Validate `desc`, build the work-unit table (blocks of 4 consecutive queries of one
  * segment, ordered longest-first), and allocate the plan's device block (unit table,
- * 16-byte ticket block, device status word) on the current device. The ticket block and
- * status word are zeroed and the unit table uploaded on `stream` (see the stream-ordering
+ * two 16-byte ticket blocks (scan, selection), device status word) on the current device.
+ * The ticket blocks and status word are zeroed and the unit table uploaded on `stream` (see the stream-ordering
  * note above). On success *out_plan owns that memory until indexer_topk_destroy().
  * Reference: flashinfer PR #8691, commit note "prepare now decides ... before it issues its
  * first device operation" and commit note "TicketWord ... ABI dsa_indexer_v4" (a runner's
@@ -101,14 +102,17 @@ typedef struct {
 ITK_API int indexer_topk_prepare(const itk_desc* desc, void* stream, itk_plan* out_plan);
 
 /* Bytes of caller-owned device workspace a run of this plan needs (0 if plan is NULL).
- * The workspace holds per-CTA candidate buffers; it need not be zeroed and its contents
- * are scratch after a run. Reference: same page, commit note "zero_region ... ABI dsa_indexer_v3" (caller-owned
+ * The workspace holds the scan's per-CTA working buffers (about 0.56 MB per CTA), the
+ * candidate store (32 KB per query slot, four slots per work unit) and its counts; it
+ * need not be zeroed and its contents are scratch after a run. Reference: same page, commit note "zero_region ... ABI dsa_indexer_v3" (caller-owned
  * workspace). */
 ITK_API size_t indexer_topk_workspace_bytes(itk_plan plan);
 
 /*
- * One scan on `stream`: exactly one kernel launch (plus a 16-byte memset only right after
- * a failed launch). Arguments:
+ * One scan on `stream`: exactly two kernel launches -- the scan, which leaves each
+ * query's candidates (a superset of its top-k, at most 4096 keys) in the workspace, then
+ * the selection, which writes the sorted top-k rows -- plus a 32-byte memset only right
+ * after a failed launch. Arguments:
  *   q          device, BF16 [T,H,D] row-major, 16-byte aligned
  *   k          device, BF16 [Tkv,D] row-major, 16-byte aligned
  *   w          device, FP32 [T,H] row-major
@@ -116,7 +120,7 @@ ITK_API size_t indexer_topk_workspace_bytes(itk_plan plan);
  *   out_scores device, FP32 [T,top_k] row-major (written)
  *   workspace  device, >= indexer_topk_workspace_bytes(plan) bytes (may be NULL if that is 0)
  * Buffers may change from run to run; a shape change needs a new plan. Runs of one plan
- * must not overlap in time (they share the plan's ticket block): issue them on one stream
+ * must not overlap in time (they share the plan's ticket blocks): issue them on one stream
  * or order them. The call is asynchronous; launch errors are returned, in-kernel wait
  * timeouts are reported by indexer_topk_device_status().
  * Reference: same page, commit note "TicketWord ... ABI dsa_indexer_v4" (ticket word, the
@@ -127,10 +131,10 @@ ITK_API int indexer_topk_run(itk_plan plan, const void* q, const void* k, const 
 
 /*
  * Eager entry: prepare + run + destroy in one call, for a one-shot scan. It allocates no
- * device memory: the unit table and the ticket block live at the end of the caller's
+ * device memory: the unit table and the ticket blocks live at the end of the caller's
  * workspace, which must hold indexer_topk_eager_workspace_bytes(desc) bytes. Device work
- * on `stream`: one host-to-device copy of the unit table with a zeroed ticket block, then
- * the scan kernel. Reference: same page, "Changes" table row "Runner entry points and
+ * on `stream`: one host-to-device copy of the unit table with zeroed ticket blocks, then
+ * the scan and selection kernels. Reference: same page, "Changes" table row "Runner entry points and
  * validation" (the eager entry uses a one-shot runner) and the TicketWord commit note (the
  * eager entry zeroes its ticket word on the launch stream).
  */
@@ -144,9 +148,10 @@ ITK_API void indexer_topk_destroy(itk_plan plan);
 
 /*
  * Wait for `stream`, then read the plan's device status word: ITK_OK, or
- * ITK_ERR_DEVICE_TIMEOUT if a bounded wait inside an earlier run of this plan gave up
- * (outputs of that run are then undefined; the next run re-zeroes the ticket block).
- * Reading clears the word.
+ * ITK_ERR_DEVICE_TIMEOUT if a bounded wait inside an earlier run of this plan gave up, or
+ * ITK_ERR_INTERNAL if a kernel found one of its own invariants broken (outputs of that
+ * run are then undefined; the next run re-zeroes the ticket blocks). Reading clears the
+ * word.
  */
 ITK_API int indexer_topk_device_status(itk_plan plan, void* stream);
 
@@ -175,16 +180,17 @@ ITK_API const char* indexer_topk_version(void);
 
 /*
  * Scan without any device allocation: same operation, arguments and output as
- * indexer_topk_prepare + indexer_topk_run, but every byte of scratch (candidate buffers,
- * work-unit table, ticket block, status word) lives in one static device array of
- * indexer_topk_noalloc_scratch_bytes() bytes (about 86 MB) that every GPU loading this
- * library holds until the process exits. The paper has no counterpart: it exists for
+ * indexer_topk_prepare + indexer_topk_run, but every byte of scratch (working buffers,
+ * candidate store, work-unit table, ticket blocks, status word) lives in one static
+ * device array of indexer_topk_noalloc_scratch_bytes() bytes (about 153 MB) that every
+ * GPU loading this library holds until the process exits. The store holds 512 work units
+ * (2048 queries); larger inputs run as one scan + selection launch pair per 512 units. The paper has no counterpart: it exists for
  * callers that must not call cudaMalloc at call time -- a serving runtime or framework
  * that has already reserved the device memory for its own pool, or a latency-critical
  * path where an allocation, which can synchronize the device, is not acceptable.
  *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call. The
- *     work-unit table is copied from host memory and the ticket block and status word
- *     are zeroed on `stream` before the scan; the candidate buffers need no clearing.
+ *     work-unit table is copied from host memory and the ticket blocks and status word
+ *     are zeroed on `stream` before the scan; working buffers and store need no clearing.
  *   - Limits: at most 65536 work units (4 consecutive queries of one segment each, so
  *     about 262144 queries), and at most 152 CTAs; larger descriptors are rejected with
  *     ITK_ERR_UNSUPPORTED and a message from indexer_topk_last_error().

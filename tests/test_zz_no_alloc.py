@@ -54,7 +54,9 @@ def test_noalloc_matches_prepared_on_two_calls(env):
     cu_k = np.array([0, 2600, 4000], np.int32)
     first = inputs.draw(1500, 4000, cu_q, cu_k, 512, q_causal_offsets=[1900, 500], seed=31, kind="normal")
     second = inputs.draw(900, 900, [0, 900], [0, 900], 256, seed=32, kind="int")
-    for wl in (first, second):
+    # more than 512 work units: the static candidate store takes them in two launch pairs
+    third = inputs.draw(2600, 3000, [0, 1300, 2600], [0, 1500, 3000], 128, seed=33, kind="normal")
+    for wl in (first, second, third):
         q, k, w = parity.to_device(wl, dev)
         ref_ids, ref_sc = _prepared(binding, torch, dev, wl, q, k, w)
         got_ids, got_sc = _noalloc(binding, torch, dev, wl, q, k, w)
