@@ -14,14 +14,15 @@
 // (each running CTA takes the next unit, so a CTA that cannot start does not hold back a
 // second wave) and the TicketWord note (every completed scan leaves the word at zero).
 //
-// CTA layout (320 threads, one CTA per SM):
+// CTA layout (576 threads, one CTA per SM):
 //   warp 0        ticket draws, TMA loads of the Q block and of the K tile ring
 //   warp 1        TMEM allocation, tcgen05.mma issue (one thread)
-//   warps 2..9    epilogue: two groups of four warps; group g owns queries 2g, 2g+1 of
-//                 the unit; the four warps of a group cover the 128 TMEM lanes (keys).
-//                 Per key tile: scores, candidate filter, appends to the query's
-//                 working buffer, histogram of the appended score keys; at the end of
-//                 the unit, the hand-off to the candidate store.
+//   warps 2..17   epilogue: four groups of four warps; group g owns query g of the unit;
+//                 the four warps of a group cover the 128 TMEM lanes (keys), so every
+//                 SM sub-partition runs four epilogue warps. Per key tile: scores,
+//                 candidate filter, appends to the query's working buffer, histogram of
+//                 the appended score keys; at the end of the unit, the hand-off to the
+//                 candidate store.
 //
 // Score arithmetic (fixed, so a score depends only on q[t], k[s] and w[t], never on
 // tiling, unit or CTA): the tensor core forms the FP32 dot products x_h = q[t,h,:].k[s,:]
@@ -47,11 +48,12 @@ namespace itk {
 constexpr int kN = kQB * kHeads;             // MMA N = 256 (query, head) columns
 constexpr int kStages = 3;                   // K tile ring depth
 constexpr int kQCap = 16384;                 // working buffer entries per query while a unit runs
-constexpr int kSyncEvery = 16;               // epilogue group synchronizes every this many tiles
+constexpr int kSyncEvery = 32;               // epilogue group synchronizes every this many tiles
 constexpr uint32_t kCompactAt = kQCap - kSyncEvery * kBlockKeys;  // buffer fill that triggers a compaction
-constexpr int kNumWarps = 10;
+constexpr int kEpiGroups = kQB;              // one 4-warp epilogue group per query of the unit
+constexpr int kEpiWarps = 4 * kEpiGroups;
+constexpr int kNumWarps = 2 + kEpiWarps;
 constexpr int kNumThreads = kNumWarps * 32;
-constexpr int kEpiWarps = 8;
 constexpr int kFirstEpiWarp = 2;
 constexpr uint32_t kTmemCols = 512;          // two accumulator buffers of 256 columns
 
@@ -65,10 +67,10 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
 constexpr uint32_t kOffHist = kOffK + kStages * kKStageBytes;          // 4 queries x 1024 words (2 x u16 bins)
 constexpr uint32_t kOffW = kOffHist + kQB * (kBins / 2) * 4;           // 4 queries x 64 floats
-constexpr uint32_t kOffRadix = kOffW + kQB * kHeads * 4;               // 2 groups x 256 x u32
-constexpr uint32_t kOffQState = kOffRadix + 2 * 256 * 4;               // 4 queries x 4 x u32
-constexpr uint32_t kOffSel = kOffQState + kQB * 16;                    // 2 groups x 8 x u32
-constexpr uint32_t kOffUnit = kOffSel + 2 * 8 * 4;                     // 2 slots x (int4 unit, int unit index)
+constexpr uint32_t kOffRadix = kOffW + kQB * kHeads * 4;               // 4 groups x 256 x u32
+constexpr uint32_t kOffQState = kOffRadix + kEpiGroups * 256 * 4;      // 4 queries x 4 x u32
+constexpr uint32_t kOffSel = kOffQState + kQB * 16;                    // 4 groups x 8 x u32
+constexpr uint32_t kOffUnit = kOffSel + kEpiGroups * 8 * 4;            // 2 slots x (int4 unit, int unit index)
 constexpr uint32_t kOffBar = kOffUnit + 2 * 32;                        // mbarriers
 constexpr uint32_t kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;                  // tmem base, abort, flags
@@ -89,12 +91,12 @@ struct ScanParams {
   TicketBlock* ticket;
   uint32_t* status;              // device status word (0 = ok)
   const float* w;                // [T,64]
-  unsigned long long* cand;      // per CTA: 4 x kQCap working keys, then 2 x kMaxTopK exact-select scratch
+  unsigned long long* cand;      // per CTA: 4 x kQCap working keys, then 4 x kMaxTopK exact-select scratch
   unsigned long long* store;     // [n_units * 4][kCap] candidate keys handed to the selection kernel
   uint32_t* counts;              // [n_units * 4] keys in each store slot
 };
 
-constexpr size_t kCandKeysPerCta = static_cast<size_t>(kQB) * kQCap + 2 * kMaxTopK;
+constexpr size_t kCandKeysPerCta = static_cast<size_t>(kQB) * kQCap + kEpiGroups * kMaxTopK;
 __host__ __device__ constexpr size_t candidate_bytes_per_cta() { return kCandKeysPerCta * sizeof(unsigned long long); }
 // Candidate store bytes per work unit (four query slots of kCap keys, then the counts live apart).
 __host__ __device__ constexpr size_t store_bytes_per_unit() {
@@ -203,7 +205,7 @@ __device__ uint32_t group_exact_in_place(const GroupCtx& c, unsigned long long* 
 // rewritten); returns the number that qualified (callers make sure it is <= limit).
 __device__ __forceinline__ uint32_t group_drop_below(const GroupCtx& c, unsigned long long* buf, uint32_t n,
                                                      uint32_t thr, unsigned long long* dst, uint32_t limit,
-                                                     uint32_t* s_pos, uint64_t pol) {
+                                                     uint32_t* s_pos, uint64_t pol_src, uint64_t pol_dst) {
   constexpr int kChunk = 16;  // keys per thread per pass
   if (c.gtid == 0) *s_pos = 0u;
   gsync(c);
@@ -212,7 +214,7 @@ __device__ __forceinline__ uint32_t group_drop_below(const GroupCtx& c, unsigned
 #pragma unroll
     for (int r = 0; r < kChunk; ++r) {
       const uint32_t idx = base + c.gtid + 128u * r;
-      x[r] = idx < n ? ld_hint_u64(buf + idx, pol) : 0ull;
+      x[r] = idx < n ? ld_hint_u64(buf + idx, pol_src) : 0ull;
     }
     gsync(c);
 #pragma unroll
@@ -220,7 +222,7 @@ __device__ __forceinline__ uint32_t group_drop_below(const GroupCtx& c, unsigned
       const uint32_t idx = base + c.gtid + 128u * r;
       const bool keep = idx < n && bin_of(x[r]) >= thr;
       const uint32_t slot = warp_append_slot(keep, s_pos, c.lane);
-      if (keep && slot < limit) st_hint_u64(dst + slot, x[r], pol);
+      if (keep && slot < limit) st_hint_u64(dst + slot, x[r], pol_dst);
     }
   }
   gsync(c);
@@ -236,7 +238,7 @@ __device__ __forceinline__ uint32_t group_drop_below(const GroupCtx& c, unsigned
 __device__ __forceinline__ void epi_compact(const GroupCtx& c, unsigned long long* buf, uint32_t* qs, uint32_t* hist,
                                             uint32_t K, uint32_t* s_pos, uint64_t pol, uint32_t limit,
                                             unsigned long long* scratch) {
-  uint32_t m = group_drop_below(c, buf, qs[0], qs[2], buf, kQCap, s_pos, pol);
+  uint32_t m = group_drop_below(c, buf, qs[0], qs[2], buf, kQCap, s_pos, pol, pol);
   if (m > limit) {
     const uint32_t t = group_exact_in_place(c, buf, m, hist, K, s_pos, scratch);
     m = K;
@@ -254,15 +256,15 @@ __device__ __forceinline__ void epi_compact(const GroupCtx& c, unsigned long lon
 // at or above the threshold, or exactly the K largest when more than kCap of those
 // remain) go to its store slot, and their number to *count.
 __device__ __forceinline__ void epi_handoff(const GroupCtx& c, unsigned long long* buf, const uint32_t* qs, uint32_t K,
-                                            uint32_t* s_pos, uint64_t pol, unsigned long long* dst, uint32_t* count,
-                                            uint32_t* status) {
+                                            uint32_t* s_pos, uint64_t pol_src, uint64_t pol_dst, unsigned long long* dst,
+                                            uint32_t* count, uint32_t* status) {
   const uint32_t n = qs[0];
   uint32_t m;
   if (qs[3] > static_cast<uint32_t>(kCap)) {  // uniform; qs[3] counts the keys at or above the threshold bin
     const unsigned long long prefix = group_select_stream(c, buf, n, K);
     m = group_keep_at_or_above(c, buf, n, prefix, dst, K, s_pos);
   } else {
-    m = group_drop_below(c, buf, n, qs[2], dst, kCap, s_pos, pol);
+    m = group_drop_below(c, buf, n, qs[2], dst, kCap, s_pos, pol_src, pol_dst);
   }
   if (c.gtid == 0) {
     if (m > static_cast<uint32_t>(kCap)) {  // cannot happen: qs[3] is the exact number kept
@@ -331,8 +333,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   uint32_t* s_misc = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   uint32_t* s_tmem = s_misc + 0;
   volatile uint32_t* s_abort = s_misc + 1;
-  uint32_t* s_gfail = s_misc + 2;  // [2] per-group failure flags
-  uint32_t* s_pos = s_misc + 6;    // [2] epilogue-group cursors
+  uint32_t* s_gfail = s_misc + 2;  // [4] per-group failure flags
+  uint32_t* s_pos = s_misc + 6;    // [4] epilogue-group cursors
 
   const uint32_t bar0 = smem_u32(smem + kOffBar);
   Bars bars;
@@ -493,7 +495,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else {
     // ---------------------------------------------------------------- epilogue
     const int ew = warp - kFirstEpiWarp;
-    const int g = ew >> 2;
+    const int g = ew >> 2;  // the query of the unit this group owns
     GroupCtx c;
     c.gwarp = ew & 3;
     c.lane = lane;
@@ -505,10 +507,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const int key_lane = quarter * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t K = static_cast<uint32_t>(p.top_k);
-    const uint64_t pol_cand = policy_evict_last();
-    uint32_t* hist_g = reinterpret_cast<uint32_t*>(smem + kOffHist) + (2 * g) * (kBins / 2);
-    unsigned long long* cand = p.cand + static_cast<size_t>(blockIdx.x) * kCandKeysPerCta;
-    unsigned long long* exact_scratch = cand + static_cast<size_t>(kQB) * kQCap + g * kMaxTopK;
+    const uint64_t pol_cand = policy_evict_last();   // working buffers: reused unit after unit
+    const uint64_t pol_store = policy_evict_first();  // candidate store: read only by the next kernel
+    uint32_t* hist_g = reinterpret_cast<uint32_t*>(smem + kOffHist) + g * (kBins / 2);
+    uint32_t* qs = s_qs + g * 4;
+    const float4* wv = reinterpret_cast<const float4*>(s_w + g * kHeads);
+    unsigned long long* cand = p.cand + static_cast<size_t>(blockIdx.x) * kCandKeysPerCta + static_cast<size_t>(g) * kQCap;
+    unsigned long long* exact_scratch =
+        p.cand + static_cast<size_t>(blockIdx.x) * kCandKeysPerCta + static_cast<size_t>(kQB) * kQCap + g * kMaxTopK;
+    // The groups' sync points are spread over the kSyncEvery tiles, so that the MMA never
+    // waits for all four groups at once.
+    const int sync_phase = g * (kSyncEvery / kEpiGroups);
 
     uint32_t it = 0, ac = 0;
     while (true) {
@@ -523,37 +532,33 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       if (s_gfail[g]) break;
       const int4 unit = s_unit[2 * slot];
       if (unit.x < 0) break;
+      const bool active = g < unit.y;  // uniform across the group
       const size_t uidx = static_cast<size_t>(s_unit[2 * slot + 1].x);
-      for (int i = c.gtid; i < 2 * kHeads; i += 128) {
-        const int j = 2 * g + i / kHeads, h = i % kHeads;
-        s_w[j * kHeads + h] = j < unit.y ? p.w[static_cast<size_t>(unit.x + j) * kHeads + h] : 0.f;
-      }
-      for (int i = c.gtid; i < kBins; i += 128) hist_g[i] = 0u;  // both queries' packed bins
-      if (c.gtid < 8) s_qs[(2 * g) * 4 + c.gtid] = 0u;
+      if (c.gtid < kHeads) s_w[g * kHeads + c.gtid] = active ? p.w[static_cast<size_t>(unit.x + g) * kHeads + c.gtid] : 0.f;
+      for (int i = c.gtid; i < kBins / 2; i += 128) hist_g[i] = 0u;
+      if (c.gtid < 4) qs[c.gtid] = 0u;
       gsync(c);
       const int nt = n_tiles_of(unit);
+      const int last_key = unit.w + g;  // causal bound: local keys 0..last_key are visible
       bool failed = false;
+      uint32_t thr = 0u;  // threshold bin, refreshed at every sync point
       for (int tile = 0; tile < nt; ++tile, ++ac) {
         const int ab = ac & 1;
-        if (tile % kSyncEvery == 0) {
+        if (tile % kSyncEvery == sync_phase) {
           // Group sync point (the only barriers inside a unit): every append of the
-          // earlier tiles is done, so counts and histograms are final.
+          // earlier tiles is done, so the count and the histogram are final.
           gsync(c);
           if (s_gfail[g]) {  // uniform: read after the barrier
             failed = true;
             break;
           }
-          // warp jj raises query 2g+jj's threshold bin
-          if (tile > 0 && c.gwarp < 2 && 2 * g + c.gwarp < unit.y)
-            warp_raise_threshold(s_qs + (2 * g + c.gwarp) * 4, hist_g + c.gwarp * (kBins / 2), K, lane);
-          gsync(c);
-          // make room for the appends of the next kSyncEvery tiles (uniform decision)
-#pragma unroll 1
-          for (int jj = 0; jj < 2; ++jj) {
-            const int j = 2 * g + jj;
-            if (j < unit.y && s_qs[j * 4] > kCompactAt)
-              epi_compact(c, cand + static_cast<size_t>(j) * kQCap, s_qs + j * 4, hist_g + jj * (kBins / 2), K,
-                          &s_pos[g], pol_cand, kCompactAt, exact_scratch);
+          if (active) {
+            if (c.gwarp == 0) warp_raise_threshold(qs, hist_g, K, lane);
+            gsync(c);
+            // make room for the appends of the next kSyncEvery tiles (uniform decision)
+            if (qs[0] > kCompactAt)
+              epi_compact(c, cand, qs, hist_g, K, &s_pos[g], pol_cand, kCompactAt, exact_scratch);
+            thr = qs[2];
           }
         }
         if (!mbar_wait(bars.af(ab), (ac >> 1) & 1, s_abort)) {
@@ -563,87 +568,65 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         tc_fence_after_sync();
         const int jl = tile * kBlockKeys + key_lane;  // local key index within the segment
-        uint32_t key32[2] = {0u, 0u};
+        uint32_t key32 = 0u;
+        if (active) {
+          const uint32_t col = static_cast<uint32_t>(ab * kN + g * kHeads);
+          float ps[8];
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * g + jj;
-          if (j < unit.y) {  // uniform across the group
-            const uint32_t col = static_cast<uint32_t>(ab * kN + j * kHeads);
-            const float4* wv = reinterpret_cast<const float4*>(s_w + j * kHeads);
-            float ps[8];
+          for (int m = 0; m < 8; ++m) ps[m] = 0.f;
 #pragma unroll
-            for (int m = 0; m < 8; ++m) ps[m] = 0.f;
+          for (int half = 0; half < 2; ++half) {  // heads 32 half .. 32 half + 31
+            uint32_t x[32];
+            tmem_ld32(lane_addr + col + 32 * half, x);
+            tmem_ld_wait();
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {  // heads 32 half .. 32 half + 31
-              uint32_t x[32];
-              tmem_ld32(lane_addr + col + 32 * half, x);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {  // heads 32 half + 8i .. + 7
-                const float4 wa = wv[8 * half + 2 * i];
-                const float4 wb = wv[8 * half + 2 * i + 1];
-                const float r0 = fmaxf(__uint_as_float(x[8 * i + 0]), 0.f);
-                const float r1 = fmaxf(__uint_as_float(x[8 * i + 1]), 0.f);
-                const float r2 = fmaxf(__uint_as_float(x[8 * i + 2]), 0.f);
-                const float r3 = fmaxf(__uint_as_float(x[8 * i + 3]), 0.f);
-                const float r4 = fmaxf(__uint_as_float(x[8 * i + 4]), 0.f);
-                const float r5 = fmaxf(__uint_as_float(x[8 * i + 5]), 0.f);
-                const float r6 = fmaxf(__uint_as_float(x[8 * i + 6]), 0.f);
-                const float r7 = fmaxf(__uint_as_float(x[8 * i + 7]), 0.f);
-                ffma2(ps[0], ps[1], wa.x, wa.y, r0, r1);
-                ffma2(ps[2], ps[3], wa.z, wa.w, r2, r3);
-                ffma2(ps[4], ps[5], wb.x, wb.y, r4, r5);
-                ffma2(ps[6], ps[7], wb.z, wb.w, r6, r7);
-              }
+            for (int i = 0; i < 4; ++i) {  // heads 32 half + 8i .. + 7
+              const float4 wa = wv[8 * half + 2 * i];
+              const float4 wb = wv[8 * half + 2 * i + 1];
+              const float r0 = fmaxf(__uint_as_float(x[8 * i + 0]), 0.f);
+              const float r1 = fmaxf(__uint_as_float(x[8 * i + 1]), 0.f);
+              const float r2 = fmaxf(__uint_as_float(x[8 * i + 2]), 0.f);
+              const float r3 = fmaxf(__uint_as_float(x[8 * i + 3]), 0.f);
+              const float r4 = fmaxf(__uint_as_float(x[8 * i + 4]), 0.f);
+              const float r5 = fmaxf(__uint_as_float(x[8 * i + 5]), 0.f);
+              const float r6 = fmaxf(__uint_as_float(x[8 * i + 6]), 0.f);
+              const float r7 = fmaxf(__uint_as_float(x[8 * i + 7]), 0.f);
+              ffma2(ps[0], ps[1], wa.x, wa.y, r0, r1);
+              ffma2(ps[2], ps[3], wa.z, wa.w, r2, r3);
+              ffma2(ps[4], ps[5], wb.x, wb.y, r4, r5);
+              ffma2(ps[6], ps[7], wb.z, wb.w, r6, r7);
             }
-            const float score =
-                (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]))) + 0.0f;
-            key32[jj] = ord_key(score);
           }
+          const float score = (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]))) + 0.0f;
+          key32 = ord_key(score);
         }
         // the accumulator buffer is read: hand it back to the MMA
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.ae(ab));
-        // appends: both queries' slot reservations are issued before either is used
-        bool ins[2];
-        uint32_t m[2], base[2] = {0u, 0u};
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * g + jj;
-          ins[jj] = j < unit.y && jl <= unit.w + j && (key32[jj] >> kBinShift) >= s_qs[j * 4 + 2];
-          m[jj] = __ballot_sync(0xFFFFFFFFu, ins[jj]);
-        }
-        const int lead0 = __ffs(m[0]) - 1, lead1 = __ffs(m[1]) - 1;
-        if (m[0] && lane == lead0) base[0] = atomicAdd(&s_qs[(2 * g) * 4], static_cast<uint32_t>(__popc(m[0])));
-        if (m[1] && lane == lead1) base[1] = atomicAdd(&s_qs[(2 * g + 1) * 4], static_cast<uint32_t>(__popc(m[1])));
-        if (m[0]) base[0] = __shfl_sync(0xFFFFFFFFu, base[0], lead0);
-        if (m[1]) base[1] = __shfl_sync(0xFFFFFFFFu, base[1], lead1);
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          if (ins[jj]) {
-            const int j = 2 * g + jj;
-            st_hint_u64(cand + static_cast<size_t>(j) * kQCap + base[jj] + __popc(m[jj] & ((1u << lane) - 1u)),
-                        (static_cast<unsigned long long>(key32[jj]) << 32) | static_cast<uint32_t>(unit.z + jl),
-                        pol_cand);
-            hist16_inc(hist_g + jj * (kBins / 2), key32[jj] >> kBinShift);
+        // append the keys that pass the filter
+        const bool ins = active && jl <= last_key && (key32 >> kBinShift) >= thr;
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, ins);
+        if (m) {
+          const int lead = __ffs(m) - 1;
+          uint32_t base = 0u;
+          if (lane == lead) base = atomicAdd(&qs[0], static_cast<uint32_t>(__popc(m)));
+          base = __shfl_sync(0xFFFFFFFFu, base, lead);
+          if (ins) {
+            st_hint_u64(cand + base + __popc(m & ((1u << lane) - 1u)),
+                        (static_cast<unsigned long long>(key32) << 32) | static_cast<uint32_t>(unit.z + jl), pol_cand);
+            hist16_inc(hist_g, key32 >> kBinShift);
           }
         }
       }
       if (failed) break;
-      // Hand-off: every candidate of the unit's queries goes to the store.
+      // Hand-off: every candidate of the unit's query goes to the store.
       gsync(c);  // every append of the unit is done
-      if (c.gwarp < 2 && 2 * g + c.gwarp < unit.y)
-        warp_raise_threshold(s_qs + (2 * g + c.gwarp) * 4, hist_g + c.gwarp * (kBins / 2), K, lane);
-      gsync(c);
-#pragma unroll 1
-      for (int jj = 0; jj < 2; ++jj) {
-        const int j = 2 * g + jj;
-        if (j < unit.y) {  // uniform
-          const size_t item = uidx * kQB + j;
-          epi_handoff(c, cand + static_cast<size_t>(j) * kQCap, s_qs + j * 4, K, &s_pos[g], pol_cand,
-                      p.store + item * kCap, p.counts + item, p.status);
-        }
+      if (active) {
+        if (c.gwarp == 0) warp_raise_threshold(qs, hist_g, K, lane);
+        gsync(c);
+        const size_t item = uidx * kQB + g;
+        epi_handoff(c, cand, qs, K, &s_pos[g], pol_cand, pol_store, p.store + item * kCap, p.counts + item, p.status);
       }
       gsync(c);
       __syncwarp();

@@ -31,9 +31,12 @@ constexpr int kStageSlack = 256;              // staging slots past top_k
 constexpr int kBigBucket = 32;                // sub-buckets above this size take the full sort
 
 // Per-group shared memory of the selection kernel (offsets within the group's slice).
-constexpr uint32_t kSgBins = 0;                                        // 2048 x u32
-constexpr uint32_t kSgSub = kSgBins + kBins * 4;                       // 4096 x u32
-constexpr uint32_t kSgStage = kSgSub + kCap * 4;                       // (2048 + 256) x u64
+// The bin and sub-bucket arrays carry one pad word per run of entries that one thread
+// scans (16 bins, 32 sub-buckets), so that the 32 lanes of a warp, each walking its own
+// run, hit 32 different banks.
+constexpr uint32_t kSgBins = 0;                                        // 2048 + 128 x u32
+constexpr uint32_t kSgSub = kSgBins + (kBins + kBins / 16) * 4;        // 4096 + 128 x u32
+constexpr uint32_t kSgStage = kSgSub + (kCap + kCap / 32) * 4;         // (2048 + 256) x u64
 constexpr uint32_t kSgRadix = kSgStage + (kMaxTopK + kStageSlack) * 8; // 256 x u32
 constexpr uint32_t kSgSel = kSgRadix + 256 * 4;                        // 8 x u32
 constexpr uint32_t kSgFlags = kSgSel + 8 * 4;                          // 4 x u32
@@ -42,6 +45,9 @@ constexpr uint32_t kSgBytes = (kSgItem + 16 + 127) / 128 * 128;
 constexpr uint32_t kSelSmemBytes = kSelGroups * kSgBytes;
 static_assert(kSgStage % 16 == 0, "alignment");
 static_assert(kSelSmemBytes <= 232448, "shared memory budget");
+
+__device__ __forceinline__ uint32_t bin_pad(uint32_t b) { return b + (b >> 4); }
+__device__ __forceinline__ uint32_t sub_pad(uint32_t i) { return i + (i >> 5); }
 
 struct SelectParams {
   const UnitDesc* units;              // the scan's unit table; item i is query i % 4 of unit i / 4
@@ -55,16 +61,14 @@ struct SelectParams {
   float* out_scores;                  // [T, top_k]
 };
 
-// Exclusive prefix sum of a[0..n) in place (n <= 128 * kPer), 128 threads; returns the total.
-template <int kPer>
-__device__ __forceinline__ uint32_t group_exclusive_scan(const GroupCtx& c, uint32_t* a, uint32_t n) {
-  uint32_t loc[kPer];
+// Exclusive prefix sum of the padded array a (entry i at a[sub_pad(i)], i < n <= 128 *
+// kPerThread) in place, 128 threads, each scanning a run of kPerThread entries.
+__device__ __forceinline__ void group_exclusive_scan_padded(const GroupCtx& c, uint32_t* a, uint32_t n) {
   uint32_t s = 0;
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const uint32_t idx = c.gtid * kPer + i;
-    loc[i] = idx < n ? a[idx] : 0u;
-    s += loc[i];
+  for (int i = 0; i < kPerThread; ++i) {
+    const uint32_t idx = c.gtid * kPerThread + i;
+    s += idx < n ? a[sub_pad(idx)] : 0u;
   }
   uint32_t incl = s;
 #pragma unroll
@@ -74,22 +78,19 @@ __device__ __forceinline__ uint32_t group_exclusive_scan(const GroupCtx& c, uint
   }
   if (c.lane == 31) c.sel[4 + c.gwarp] = incl;
   gsync(c);
-  uint32_t base = 0, total = 0;
+  uint32_t run = incl - s;
 #pragma unroll
-  for (int wv = 0; wv < 4; ++wv) {
-    const uint32_t x = c.sel[4 + wv];
-    base += wv < c.gwarp ? x : 0u;
-    total += x;
-  }
-  uint32_t run = base + incl - s;
+  for (int wv = 0; wv < 4; ++wv) run += wv < c.gwarp ? c.sel[4 + wv] : 0u;
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const uint32_t idx = c.gtid * kPer + i;
-    if (idx < n) a[idx] = run;
-    run += loc[i];
+  for (int i = 0; i < kPerThread; ++i) {  // second pass: the run is read again, not held
+    const uint32_t idx = c.gtid * kPerThread + i;
+    if (idx < n) {
+      const uint32_t x = a[sub_pad(idx)];
+      a[sub_pad(idx)] = run;
+      run += x;
+    }
   }
   gsync(c);
-  return total;
 }
 
 // Bitonic sort (descending) of a[0..np2) in shared memory, np2 a power of two.
@@ -111,28 +112,59 @@ __device__ void group_bitonic_desc(const GroupCtx& c, unsigned long long* a, uin
   }
 }
 
-// Slot-range index (in descending key order) of a kept key. ge[b] counts kept candidates
-// in bins >= b; bin b's keys own sub-buckets [ge[b+1], ge[b]) by linear position inside
-// the bin (higher key first).
-__device__ __forceinline__ uint32_t sub_bucket(const uint32_t* ge, unsigned long long x) {
-  const uint32_t b = bin_of(x);
-  const uint32_t above = b + 1 < static_cast<uint32_t>(kBins) ? ge[b + 1] : 0u;
-  const uint32_t cb = ge[b] - above;
-  const uint32_t frac = static_cast<uint32_t>(x >> 32) & ((1u << kBinShift) - 1u);  // position inside the bin
-  const uint32_t sub = ((frac >> 9) * cb) >> (kBinShift - 9);                       // 0 .. cb-1
+// Slot-range index (in descending key order) of a kept candidate with score key h (the
+// high word of its 64-bit key). ge[bin_pad(b)] counts kept candidates in bins >= b; bin
+// b's keys own sub-buckets [ge(b+1), ge(b)) by linear position inside the bin (higher key
+// first).
+__device__ __forceinline__ uint32_t sub_bucket(const uint32_t* ge, uint32_t h) {
+  const uint32_t b = h >> kBinShift;
+  const uint32_t above = b + 1 < static_cast<uint32_t>(kBins) ? ge[bin_pad(b + 1)] : 0u;
+  const uint32_t cb = ge[bin_pad(b)] - above;
+  const uint32_t frac = h & ((1u << kBinShift) - 1u);         // position inside the bin
+  const uint32_t sub = ((frac >> 9) * cb) >> (kBinShift - 9);  // 0 .. cb-1
   return above + (cb - 1u - sub);
 }
 
+// Exact fallback for the one sub-bucket that crosses position keff and is too large to
+// sort in place (heavy ties): its `need` largest keys (bit r of in_b marks this thread's
+// members, entry gtid + 128 r of buf) go to stage[start ..), unsorted. Kept out of line so
+// that its 64-bit key registers do not weigh on the common path.
+__device__ __noinline__ void sel_crossing_fallback(const GroupCtx& c, const unsigned long long* buf, uint32_t n,
+                                                   uint32_t in_b, uint32_t need, uint32_t start,
+                                                   unsigned long long* stage, uint32_t* flags) {
+  unsigned long long v[kPerThread];
+  group_load(c, buf, n, v);
+  const unsigned long long pfx = group_select(c, v, in_b, need);
+  if (c.gtid == 0) flags[3] = start;
+  gsync(c);
+#pragma unroll
+  for (int r = 0; r < kPerThread; ++r) {
+    const bool take = ((in_b >> r) & 1u) && v[r] >= pfx;
+    const uint32_t slot = warp_append_slot(take, &flags[3], c.lane);
+    if (take && slot < start + need) stage[slot] = v[r];  // exactly `need` keys qualify: keys are distinct
+  }
+  gsync(c);
+}
+
 // Exact top-k of one query's n candidates (buf[0..n), n <= kCap), sorted by the total
-// order, written as one output row.
+// order, written as one output row. Each thread holds the score keys (high words) of
+// candidates gtid + 128 r in registers; full 64-bit keys are read again from buf only to
+// place them.
 __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned long long* buf, uint32_t n,
                                            uint32_t top_k, uint32_t* ge, uint32_t* sub, unsigned long long* stage,
                                            uint32_t* flags, int32_t* out_ids, float* out_scores) {
-  unsigned long long v[kPerThread];
-  const uint32_t valid = group_load(c, buf, n, v);
+  const uint32_t* buf_hi = reinterpret_cast<const uint32_t*>(buf) + 1;  // high word of entry i at buf_hi[2 i]
+  uint32_t hk[kPerThread];
+  uint32_t valid = 0;
+#pragma unroll
+  for (int r = 0; r < kPerThread; ++r) {
+    const uint32_t idx = c.gtid + 128u * r;
+    hk[r] = idx < n ? buf_hi[2 * idx] : 0u;
+    valid |= (idx < n ? 1u : 0u) << r;
+  }
   const uint32_t keff = n < top_k ? n : top_k;
   // count the candidates per bin
-  for (int i = c.gtid; i < kBins; i += 128) ge[i] = 0u;
+  for (int i = c.gtid; i < kBins + kBins / 16; i += 128) ge[i] = 0u;
   if (c.gtid == 0) {
     flags[0] = kBins - 1;    // first kept bin
     flags[1] = 0u;           // large sub-bucket seen
@@ -141,15 +173,15 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   gsync(c);
 #pragma unroll
   for (int r = 0; r < kPerThread; ++r)
-    if ((valid >> r) & 1u) atomicAdd(&ge[bin_of(v[r])], 1u);
+    if ((valid >> r) & 1u) atomicAdd(&ge[bin_pad(hk[r] >> kBinShift)], 1u);
   gsync(c);
-  // ge[b] = candidates in bins >= b (suffix sums, 16 bins per thread, highest bins first)
+  // ge(b) = candidates in bins >= b (suffix sums, 16 bins per thread, highest bins first)
   {
     uint32_t loc[16];
     uint32_t s = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      loc[i] = ge[kBins - 1 - (16 * c.gtid + i)];
+      loc[i] = ge[bin_pad(kBins - 1 - (16 * c.gtid + i))];
       s += loc[i];
     }
     uint32_t incl = s;
@@ -170,39 +202,39 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
       // run = candidates in bins above b; bin b reaches a position below top_k iff run < top_k
       if (run < top_k) first_kept = b;
       run += loc[i];
-      ge[b] = run;
+      ge[bin_pad(b)] = run;
     }
     atomicMin(&flags[0], first_kept);
   }
   gsync(c);
   const uint32_t tstar = flags[0];
-  const uint32_t m_keep = ge[tstar];  // candidates in kept bins
-  for (uint32_t i = c.gtid; i < m_keep; i += 128) sub[i] = 0u;
+  const uint32_t m_keep = ge[bin_pad(tstar)];  // candidates in kept bins
+  for (uint32_t i = c.gtid; i < m_keep; i += 128) sub[sub_pad(i)] = 0u;
   gsync(c);
   uint32_t kept = 0;  // bit r: candidate r lies in a kept bin
 #pragma unroll
   for (int r = 0; r < kPerThread; ++r) {
-    if (((valid >> r) & 1u) && bin_of(v[r]) >= tstar) {
+    if (((valid >> r) & 1u) && (hk[r] >> kBinShift) >= tstar) {
       kept |= 1u << r;
-      atomicAdd(&sub[sub_bucket(ge, v[r])], 1u);
+      atomicAdd(&sub[sub_pad(sub_bucket(ge, hk[r]))], 1u);
     }
   }
   gsync(c);
-  group_exclusive_scan<kPerThread>(c, sub, m_keep);  // sub[i] = first slot of sub-bucket i
+  group_exclusive_scan_padded(c, sub, m_keep);  // sub(i) = first slot of sub-bucket i
   const uint32_t cap = top_k + kStageSlack;
 #pragma unroll
   for (int r = 0; r < kPerThread; ++r) {
     if ((kept >> r) & 1u) {
-      const uint32_t pos = atomicAdd(&sub[sub_bucket(ge, v[r])], 1u);
-      if (pos < cap) stage[pos] = v[r];
+      const uint32_t pos = atomicAdd(&sub[sub_pad(sub_bucket(ge, hk[r]))], 1u);
+      if (pos < cap) stage[pos] = buf[c.gtid + 128u * r];
     }
   }
   gsync(c);
-  // sub[i] is now the end of sub-bucket i; sort every sub-bucket that reaches a slot below
+  // sub(i) is now the end of sub-bucket i; sort every sub-bucket that reaches a slot below
   // top_k, in place (they hold about one key each)
   for (uint32_t i = c.gtid; i < m_keep; i += 128) {
-    const uint32_t start = i ? sub[i - 1] : 0u;
-    const uint32_t end = sub[i];
+    const uint32_t start = i ? sub[sub_pad(i - 1)] : 0u;
+    const uint32_t end = sub[sub_pad(i)];
     if (start >= keff || end - start < 2) continue;
     if (end > keff && (end > cap || end - start > static_cast<uint32_t>(kBigBucket))) {
       flags[2] = i;  // the one sub-bucket that crosses position keff, too large to sort here
@@ -225,21 +257,12 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   gsync(c);
   const uint32_t over = flags[2];
   if (over != 0xFFFFFFFFu) {
-    // exact fallback: keep the (keff - start) largest keys of the crossing sub-bucket
-    const uint32_t start = over ? sub[over - 1] : 0u;
+    const uint32_t start = over ? sub[sub_pad(over - 1)] : 0u;
     uint32_t in_b = 0;
 #pragma unroll
     for (int r = 0; r < kPerThread; ++r)
-      if (((kept >> r) & 1u) && sub_bucket(ge, v[r]) == over) in_b |= 1u << r;
-    const unsigned long long pfx = group_select(c, v, in_b, keff - start);
-    if (c.gtid == 0) flags[3] = start;
-    gsync(c);
-#pragma unroll
-    for (int r = 0; r < kPerThread; ++r) {
-      const bool take = ((in_b >> r) & 1u) && v[r] >= pfx;
-      const uint32_t slot = warp_append_slot(take, &flags[3], c.lane);
-      if (take && slot < keff) stage[slot] = v[r];  // exactly keff - start keys qualify: keys are distinct
-    }
+      if (((kept >> r) & 1u) && sub_bucket(ge, hk[r]) == over) in_b |= 1u << r;
+    sel_crossing_fallback(c, buf, n, in_b, keff - start, start, stage, flags);
     if (c.gtid == 0) flags[1] = 1u;  // the refilled range is unsorted
     gsync(c);
   }
