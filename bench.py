@@ -301,9 +301,36 @@ def _measure(binding, torch, wl, dev, steps, warmup, flush_buf):
         binding.indexer_topk_run(plan, q, k, w, ids, sc, ws, stream)
     torch.cuda.synchronize()
     plan.device_status()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    return plan, (q, k, w, ids, sc, ws), starts, ends, stream
+    return plan, (q, k, w, ids, sc, ws), stream
+
+
+KERNELS_PER_STEP = 2  # the scan kernel, then the selection kernel
+
+
+def _timed_steps(binding, torch, plan, bufs, stream, steps, flush_buf):
+    """Times `steps` runs with CUDA events on the launching stream: per step the whole call
+    (start..end) and, through the library's split event recorded between its two launches,
+    the scan kernel (start..split) and the selection kernel (split..end). The L2 is
+    flushed before every step, outside the events."""
+    starts, splits, ends = ([torch.cuda.Event(enable_timing=True) for _ in range(steps)] for _ in range(3))
+    for e in splits:  # create the events' device handles
+        e.record(stream)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush_buf.fill_(i & 0xFF)
+        binding.indexer_topk_set_split_event(plan, splits[i])
+        starts[i].record(stream)
+        binding.indexer_topk_run(plan, *bufs, stream)
+        ends[i].record(stream)
+    binding.indexer_topk_set_split_event(plan, None)
+    return starts, splits, ends
+
+
+def _step_ms(starts, splits, ends):
+    total = np.array([a.elapsed_time(b) for a, b in zip(starts, ends)])
+    scan = np.array([a.elapsed_time(b) for a, b in zip(starts, splits)])
+    sel = np.array([a.elapsed_time(b) for a, b in zip(splits, ends)])
+    return float(total.mean()), float(scan.mean()), float(sel.mean())
 
 
 def run_ours(args):
@@ -329,7 +356,7 @@ def run_ours(args):
     wl = inputs.make(args.config, seed=rank)
     flops = 2.0 * visible_pairs(wl) * wl.H * wl.D
     clocks = ClockSampler(local).__enter__()  # sampling covers warm-up through the per-config runs
-    plan, bufs, starts, ends, stream = _measure(binding, torch, wl, dev, args.steps, args.warmup, flush_buf)
+    plan, bufs, stream = _measure(binding, torch, wl, dev, args.steps, args.warmup, flush_buf)
     q, k, w, ids, sc, ws = bufs
 
     def barrier():
@@ -340,17 +367,15 @@ def run_ours(args):
     barrier()
     wall0 = time.perf_counter()
     t_timed0 = time.time()
-    for i in range(args.steps):
-        flush_buf.fill_(i & 0xFF)
-        starts[i].record(stream)
-        binding.indexer_topk_run(plan, q, k, w, ids, sc, ws, stream)
-        ends[i].record(stream)
+    starts, splits, ends = _timed_steps(binding, torch, plan, bufs, stream, args.steps, flush_buf)
     barrier()
     clocks.mark_timed(t_timed0, time.time())
     wall = time.perf_counter() - wall0
     plan.device_status()
-    per_step_ms = np.array([s.elapsed_time(e) for s, e in zip(starts, ends)])
-    ms = max_over_ranks(float(per_step_ms.mean()), dist, dev)
+    total_ms, scan_ms, sel_ms = _step_ms(starts, splits, ends)
+    ms = max_over_ranks(total_ms, dist, dev)
+    scan_ms = max_over_ranks(scan_ms, dist, dev)
+    sel_ms = max_over_ranks(sel_ms, dist, dev)
     value = job_tflops(flops, world, ms)
 
     # end to end through the public API with pinned host buffers
@@ -387,18 +412,15 @@ def run_ours(args):
     for name in [c for c in args.per_config.split(",") if c and c != args.config]:
         wl2 = inputs.make(name, seed=rank)
         f2 = 2.0 * visible_pairs(wl2) * wl2.H * wl2.D
-        plan2, b2, s2, e2, st2 = _measure(binding, torch, wl2, dev, args.steps, args.warmup, flush_buf)
-        torch.cuda.synchronize()
-        for i in range(args.steps):
-            flush_buf.fill_(i & 0xFF)
-            s2[i].record(st2)
-            binding.indexer_topk_run(plan2, *b2, st2)
-            e2[i].record(st2)
+        plan2, b2, st2 = _measure(binding, torch, wl2, dev, args.steps, args.warmup, flush_buf)
+        s2, sp2, e2 = _timed_steps(binding, torch, plan2, b2, st2, args.steps, flush_buf)
         torch.cuda.synchronize()
         plan2.device_status()
-        m2 = float(np.mean([a.elapsed_time(b) for a, b in zip(s2, e2)]))
+        m2, m2_scan, m2_sel = _step_ms(s2, sp2, e2)
         tf2 = f2 / (m2 * 1e-3) / 1e12
+        tf2_scan = f2 / (m2_scan * 1e-3) / 1e12
         per_config[name] = {"ms": m2, "tflops": tf2, "frac": tf2 / peaks["bf16_tflops"],
+                            "scan_ms": m2_scan, "scan_frac": tf2_scan / peaks["bf16_tflops"], "select_ms": m2_sel,
                             "T": wl2.T, "Tkv": wl2.Tkv}
         plan2.destroy()
         del b2
@@ -409,14 +431,15 @@ def run_ours(args):
             dist.destroy_process_group()
         return 0
 
-    achieved = flops / (ms * 1e-3) / 1e12
+    achieved = flops / (scan_ms * 1e-3) / 1e12  # the dominant kernel alone
     traffic = load_traffic()
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"],
                 "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)" if peak_src == "measured"
                 else "fallback 1.9 PFLOP/s bf16 burst",
                 "traffic": None if traffic is None else traffic["bytes_per_launch_scaled"],
-                "algorithmic_flops_per_launch": flops, "kernel": "indexer_topk_scan_kernel"}
+                "algorithmic_flops_per_launch": flops, "kernel": "indexer_topk_scan_kernel",
+                "kernel_ms": scan_ms, "step_frac": value / world / peaks["bf16_tflops"]}
     if traffic is not None:
         roofline["traffic_note"] = traffic.get("note", "")
     flops_s, dt_s, nrows, threads = cpu_oracle_sample(wl, args.cpu_budget)
@@ -427,7 +450,10 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(wl, world),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(),
-        "gpu_launches": args.steps, "per_config": per_config, "wall_s_timed_region": wall,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "kernels": {"indexer_topk_scan_kernel": {"ms": scan_ms, "launches": args.steps},
+                    "indexer_topk_select_kernel": {"ms": sel_ms, "launches": args.steps}},
+        "per_config": per_config, "wall_s_timed_region": wall,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

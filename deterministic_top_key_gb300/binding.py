@@ -84,6 +84,7 @@ def load():
         "indexer_topk_debug_inject": (ctypes.c_int, [vp, ctypes.c_int, vp]),
         "indexer_topk_run_noalloc": (ctypes.c_int, [DP, vp, vp, vp, vp, vp, vp]),
         "indexer_topk_noalloc_scratch_bytes": (sz, []),
+        "indexer_topk_set_split_event": (ctypes.c_int, [vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -215,6 +216,14 @@ def indexer_topk_run_noalloc(desc: Desc, q, k, w, out_ids, out_scores, stream=No
     calls that overlap on the GPU race; keep them on one stream or ordered."""
     _check(load().indexer_topk_run_noalloc(desc.ref(), _ptr(q), _ptr(k), _ptr(w), _ptr(out_ids), _ptr(out_scores),
                                            _stream_handle(stream)))
+
+
+def indexer_topk_set_split_event(plan: Plan, event=None):
+    """Record `event` (a torch.cuda.Event that has been recorded once, or a raw
+    cudaEvent_t handle) between the scan and the selection launch of later runs; None
+    stops it."""
+    handle = None if event is None else (event.cuda_event if hasattr(event, "cuda_event") else int(event))
+    _check(load().indexer_topk_set_split_event(plan.handle, handle))
 
 
 def indexer_topk_debug_inject(plan: Plan, what: int, stream=None):

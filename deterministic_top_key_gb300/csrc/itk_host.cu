@@ -234,7 +234,7 @@ int check_run_buffers(const Layout& L, const void* q, const void* k, const float
 // selection); `work` is laid out by work_layout(grid, n_units).
 int launch_run(const Layout& L, int grid, int sm_count, const UnitDesc* d_units, size_t n_units, TicketBlock* d_ticket,
                uint32_t* d_status, const void* q, const void* k, const float* w, int32_t* ids, float* scores,
-               void* work, cudaStream_t stream, bool force_launch_failure) {
+               void* work, cudaStream_t stream, bool force_launch_failure, cudaEvent_t split_event = nullptr) {
   CUtensorMap qmap, kmap;
   int rc = encode_rows(&qmap, q, static_cast<uint64_t>(L.T) * itk::kHeads, itk::kN);
   if (rc) return rc;
@@ -260,6 +260,10 @@ int launch_run(const Layout& L, int grid, int sm_count, const UnitDesc* d_units,
   itk::indexer_topk_scan_kernel<<<grid, itk::kNumThreads, smem, stream>>>(qmap, kmap, prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "scan launch");
+  if (split_event) {
+    e = cudaEventRecord(split_event, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "recording the split event");
+  }
   itk::SelectParams sp;
   sp.units = d_units;
   sp.n_units = static_cast<int32_t>(n_units);
@@ -289,6 +293,7 @@ struct itk_plan_s {
   BlockLayout bl;
   bool ticket_dirty = false;
   bool fail_next_launch = false;  // test hook
+  cudaEvent_t split_event = nullptr;  // recorded between the two launches when set
 };
 
 extern "C" {
@@ -406,7 +411,7 @@ int indexer_topk_run(itk_plan plan, const void* q, const void* k, const float* w
   plan->fail_next_launch = false;
   rc = launch_run(L, plan->grid, plan->dev.sm_count, reinterpret_cast<const UnitDesc*>(blk + plan->bl.units_off),
                   L.units.size(), ticket, reinterpret_cast<uint32_t*>(blk + plan->bl.status_off), q, k, w, out_ids,
-                  out_scores, workspace, s, inject);
+                  out_scores, workspace, s, inject, plan->split_event);
   plan->ticket_dirty = (rc != ITK_OK);
   return rc;
 }
@@ -481,6 +486,12 @@ int indexer_topk_device_status(itk_plan plan, void* stream) {
 //             request), as after a run that raised while launching.
 //   what = 2: write a nonzero value into the plan's two ticket blocks on `stream`, as a
 //             run that stopped midway would leave them.
+int indexer_topk_set_split_event(itk_plan plan, void* event) {
+  if (!plan) return fail(ITK_ERR_INVALID_ARGUMENT, "plan is NULL");
+  plan->split_event = static_cast<cudaEvent_t>(event);
+  return ITK_OK;
+}
+
 int indexer_topk_debug_inject(itk_plan plan, int what, void* stream) {
   if (!plan) return fail(ITK_ERR_INVALID_ARGUMENT, "plan is NULL");
   if (what == 1) {

@@ -202,6 +202,15 @@ ITK_API const char* indexer_topk_version(void);
 ITK_API int indexer_topk_run_noalloc(const itk_desc* desc, const void* q, const void* k, const float* w,
                                      int32_t* out_ids, float* out_scores, void* stream);
 
+/*
+ * Per-kernel timing: from now on, every indexer_topk_run of this plan records `event` (a
+ * cudaEvent_t owned by the caller, created on the plan's device) on the run's stream
+ * between the scan launch and the selection launch, so that events recorded by the caller
+ * before and after the run bracket each kernel. NULL stops the recording. Host only;
+ * returns ITK_ERR_INVALID_ARGUMENT for a NULL plan. Not part of the operation.
+ */
+ITK_API int indexer_topk_set_split_event(itk_plan plan, void* event);
+
 /* Size in bytes of the static scratch array used by indexer_topk_run_noalloc. */
 ITK_API size_t indexer_topk_noalloc_scratch_bytes(void);
 

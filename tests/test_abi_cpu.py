@@ -82,6 +82,12 @@ def test_unit_count_for_configs(lib):
         assert lib.indexer_topk_num_units(d.ref()) == n
 
 
+def test_host_only_entry_points_reject_null_plan(lib):
+    assert lib.indexer_topk_set_split_event(None, None) == binding.ITK_ERR_INVALID_ARGUMENT
+    assert lib.indexer_topk_workspace_bytes(None) == 0
+    assert lib.indexer_topk_status_string(binding.ITK_ERR_INTERNAL) == b"internal device check failed"
+
+
 def test_prepare_without_device_fails_cleanly(lib):
     import torch
 

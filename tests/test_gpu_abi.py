@@ -102,3 +102,24 @@ def test_empty_query_set(env):
     e = torch.empty((0, 8), dtype=torch.int32, device=dev)
     binding.indexer_topk_run(plan, q, k, w, e, e.float(), None)
     plan.destroy()
+
+
+def test_split_event_brackets_the_two_kernels(env):
+    """The plan's split event is recorded between the scan and the selection launches."""
+    binding, torch, dev, wl, (q, k, w), (r_ids, r_sc) = env
+    plan = binding.indexer_topk_prepare(wl.T, wl.Tkv, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.top_k)
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
+    ids, sc = _bufs(torch, dev, wl)
+    s = torch.cuda.current_stream()
+    a, mid, b = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    mid.record(s)  # creates the event
+    binding.indexer_topk_set_split_event(plan, mid)
+    a.record(s)
+    binding.indexer_topk_run(plan, q, k, w, ids, sc, ws)
+    b.record(s)
+    binding.indexer_topk_set_split_event(plan, None)
+    torch.cuda.synchronize()
+    t_scan, t_sel, t_all = a.elapsed_time(mid), mid.elapsed_time(b), a.elapsed_time(b)
+    assert t_scan > 0 and t_sel > 0 and abs(t_scan + t_sel - t_all) < 1e-3 + 1e-3 * t_all
+    parity.assert_exact(ids.cpu().numpy(), sc.cpu().numpy(), r_ids, r_sc)
+    plan.destroy()
