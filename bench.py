@@ -269,7 +269,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="S1")
-    ap.add_argument("--per-config", default="S2,C1,Z2", help="extra configs timed and reported in per_config ('' = none)")
+    ap.add_argument("--per-config", default="S2,C1,Z2,Z3,A1,A2,A3", help="extra configs timed and reported in per_config ('' = none)")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=20.0)
     ap.add_argument("--no-e2e", action="store_true")

@@ -4,7 +4,8 @@ This module only draws numbers. It holds none of the scan's arithmetic, so the
 CUDA path and the CPU oracle can both take their inputs from it.
 
 Shapes follow the workload rows of flashinfer PR #8691's tables (single causal
-documents S1/S2, the CP tail C1 and the packed 8 x 32k CP16 row Z2cp); the
+documents S1/S2, the CP tail C1, the packed CP16 rows Z2cp and Z3cp and the split-tail
+rows A1-A3); the
 distributions are the ones the rows are benchmarked with here: q, k ~ N(0,1)
 rounded to BF16 and w ~ N(0,1)/8 (the tiny case uses w ~ U(-1,1)). Every case
 also has an integer variant, q, k uniform over {-2..2} and w uniform over
@@ -110,19 +111,35 @@ def draw(T, Tkv, cu_seqlens_q, cu_seqlens_k, top_k, *, q_causal_offsets=None, se
                     q_causal_offsets=offs, top_k=int(top_k), meta={"seed": seed, "kind": kind, "w_dist": w_dist})
 
 
-def z2_layout(n_docs=8, doc_len=32768, chunk=1024):
-    """Packed-varlen CP rank-0 layout: per document its first and its last chunk of queries.
+def cp_rank0_layout(doc_lens, cp=16):
+    """Packed-varlen layout of context-parallel rank 0 under a zigzag split: every document
+    of length L is cut into 2 * cp chunks of L / (2 cp) tokens and rank 0 holds the first
+    and the last chunk of each.
 
-    Each query segment has its own key segment: the first chunk sees the document's
-    first ``chunk`` keys (offset 0), the last chunk sees all ``doc_len`` keys (offset
-    doc_len - chunk, the bottom-right default)."""
+    Each query segment has its own key segment: the first chunk sees the document's first
+    chunk of keys (offset 0), the last chunk sees all L keys (offset L - chunk, the
+    bottom-right default)."""
     tq, tk = [], []
-    for _ in range(n_docs):
+    for L in doc_lens:
+        chunk = L // (2 * cp)
+        assert chunk * 2 * cp == L, "document length must split into 2 * cp equal chunks"
         tq += [chunk, chunk]
-        tk += [chunk, doc_len]
+        tk += [chunk, L]
     cu_q = np.concatenate([[0], np.cumsum(tq)]).astype(np.int32)
     cu_k = np.concatenate([[0], np.cumsum(tk)]).astype(np.int32)
     return cu_q, cu_k
+
+
+def z2_layout(n_docs=8, doc_len=32768):
+    """Z2cp: 8 documents of 32768 tokens at CP16 (1024-query chunks): T = 16384, Tkv = 270336."""
+    return cp_rank0_layout([doc_len] * n_docs)
+
+
+# Z3cp ("packed 4k-64k documents, CP16 zigzag rank 0", T = 10624, Tkv = 175296). The page
+# gives the totals but not the document mix. Rank 0 holds L/16 queries and L/32 + L keys of
+# a document of length L, so T = sum(L)/16 and Tkv = 33 sum(L)/32, and both totals give
+# sum(L) = 169984. These eight lengths, 4k to 50k and multiples of 1024, have that sum.
+Z3_DOCS = (4096, 8192, 12288, 16384, 20480, 24576, 32768, 51200)
 
 
 # name -> (T, Tkv, cu_q, cu_k, offsets, top_k, w_dist, description)
@@ -145,10 +162,22 @@ def config(name: str):
         return dict(T=int(cu_q[-1]), Tkv=int(cu_k[-1]), cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, top_k=2048,
                     w_dist="normal8", q_causal_offsets=None,
                     desc="packed 8 x 32k documents, first and last 1024-query chunk of each (16 segments), top_k=2048")
+    if name == "Z3":
+        cu_q, cu_k = cp_rank0_layout(Z3_DOCS)
+        return dict(T=int(cu_q[-1]), Tkv=int(cu_k[-1]), cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, top_k=2048,
+                    w_dist="normal8", q_causal_offsets=None,
+                    desc="packed 4k-50k documents at CP16 zigzag rank 0 (16 segments), top_k=2048")
+    if name in SPLIT_TAIL:
+        tkv = SPLIT_TAIL[name]
+        return dict(T=4, Tkv=tkv, cu_seqlens_q=[0, 4], cu_seqlens_k=[0, tkv], top_k=2048, w_dist="normal8",
+                    q_causal_offsets=None, desc=f"split tail: the last 4 queries of a {tkv}-key document, top_k=2048")
     raise KeyError(name)
 
 
-CONFIG_NAMES = ("tiny", "S1", "S2", "C1", "Z2")
+# split-tail rows: 4 queries at the end of one document (bottom-right offsets)
+SPLIT_TAIL = {"A1": 22018, "A2": 30466, "A3": 41986}
+
+CONFIG_NAMES = ("tiny", "S1", "S2", "C1", "Z2", "Z3", "A1", "A2", "A3")
 
 
 def make(name: str, kind: str = "normal", seed: int = 0) -> Workload:

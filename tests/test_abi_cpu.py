@@ -76,7 +76,8 @@ def test_unit_table_covers_every_query_once_longest_first(lib):
 def test_unit_count_for_configs(lib):
     from deterministic_top_key_gb300 import inputs
 
-    for name, n in [("tiny", 128), ("S1", 2048), ("S2", 4096), ("C1", 1024), ("Z2", 4096)]:
+    for name, n in [("tiny", 128), ("S1", 2048), ("S2", 4096), ("C1", 1024), ("Z2", 4096), ("Z3", 2656),
+                    ("A1", 1), ("A2", 1), ("A3", 1)]:
         c = inputs.config(name)
         d = binding.Desc(c["T"], c["Tkv"], c["cu_seqlens_q"], c["cu_seqlens_k"], c["top_k"], c["q_causal_offsets"])
         assert lib.indexer_topk_num_units(d.ref()) == n

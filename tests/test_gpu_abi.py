@@ -123,3 +123,31 @@ def test_split_event_brackets_the_two_kernels(env):
     assert t_scan > 0 and t_sel > 0 and abs(t_scan + t_sel - t_all) < 1e-3 + 1e-3 * t_all
     parity.assert_exact(ids.cpu().numpy(), sc.cpu().numpy(), r_ids, r_sc)
     plan.destroy()
+
+
+def test_cuda_graph_capture_and_replay(env):
+    """A prepared run captured into a CUDA graph replays with bit-identical rows: both
+    launches take their arguments by value and both ticket blocks reset themselves at the
+    end of every run, so each replay starts from zero."""
+    binding, torch, dev, wl, (q, k, w), (r_ids, r_sc) = env
+    plan = binding.indexer_topk_prepare(wl.T, wl.Tkv, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.top_k)
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
+    ids, sc = _bufs(torch, dev, wl)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # first run outside the capture (kernel attributes, module load)
+        binding.indexer_topk_run(plan, q, k, w, ids, sc, ws, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        binding.indexer_topk_run(plan, q, k, w, ids, sc, ws, stream=s)
+    for _ in range(3):
+        ids.fill_(5)
+        sc.fill_(0.0)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        parity.assert_exact(ids.cpu().numpy(), sc.cpu().numpy(), r_ids, r_sc)
+    plan.device_status()
+    del g
+    plan.destroy()

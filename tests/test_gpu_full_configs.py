@@ -83,7 +83,7 @@ def dev(cuda_lib):
     return torch.device("cuda:0")
 
 
-@pytest.mark.parametrize("name", ["S1", "S2", "C1", "Z2"])
+@pytest.mark.parametrize("name", ["S1", "S2", "C1", "Z2", "Z3", "A1", "A2", "A3"])
 def test_full_config_random(name, dev, oracle_mod):
     wl = inputs.make(name)
     ids, sc = _run(wl, dev)
@@ -91,7 +91,7 @@ def test_full_config_random(name, dev, oracle_mod):
     parity.assert_close(ids, sc, wl, _sample_rows(wl))
 
 
-@pytest.mark.parametrize("name", ["S1", "S2", "C1", "Z2"])
+@pytest.mark.parametrize("name", ["S1", "S2", "C1", "Z2", "Z3", "A1", "A2", "A3"])
 def test_full_config_integer(name, dev, oracle_mod):
     wl = inputs.make(name, kind="int")
     ids, sc = _run(wl, dev)

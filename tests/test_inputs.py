@@ -42,3 +42,20 @@ def test_config_layouts():
     assert np.array_equal(np.diff(cu_k), np.array([1024, 32768] * 8))
     c1 = inputs.config("C1")
     assert c1["q_causal_offsets"] == [61440] and c1["Tkv"] - c1["T"] == 61440
+
+
+def test_z3_and_split_tail_layouts():
+    """Z3cp totals as printed in the pages' table; every document splits into 32 chunks;
+    the split-tail rows are the last 4 queries of one document."""
+    c = inputs.config("Z3")
+    assert c["T"] == 10624 and c["Tkv"] == 175296
+    cu_q, cu_k = np.asarray(c["cu_seqlens_q"]), np.asarray(c["cu_seqlens_k"])
+    assert len(cu_q) == 17
+    tq, tk = np.diff(cu_q), np.diff(cu_k)
+    docs = np.asarray(inputs.Z3_DOCS)
+    assert np.array_equal(tq, np.repeat(docs // 32, 2))
+    assert np.array_equal(tk[0::2], docs // 32) and np.array_equal(tk[1::2], docs)
+    assert 4096 <= docs.min() and docs.max() <= 65536
+    for name, tkv in (("A1", 22018), ("A2", 30466), ("A3", 41986)):
+        a = inputs.config(name)
+        assert a["T"] == 4 and a["Tkv"] == tkv and a["q_causal_offsets"] is None
