@@ -201,7 +201,7 @@ def indexer_topk_unit_table(desc: Desc):
     n = int(lib.indexer_topk_num_units(desc.ref()))
     if n < 0:
         _check(-n)
-    out = np.zeros((max(n, 1), 4), np.int32)
+    out = np.zeros((max(n, 1), 6), np.int32)
     m = int(lib.indexer_topk_unit_table(desc.ref(), out.ctypes.data, n))
     if m < 0:
         _check(-m)

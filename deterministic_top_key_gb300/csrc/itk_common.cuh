@@ -39,6 +39,18 @@ struct UnitDesc {
   int32_t nq;        // queries in the unit (1..4)
   int32_t key_row0;  // first key row of the unit's segment
   int32_t pos0;      // causal position of the first query within its segment
+  int32_t tile0;     // key tiles [tile0, tile1) of the segment that this unit scans
+  int32_t tile1;     //   (all visible tiles, or one chunk of a split query block)
+};
+
+// A query whose visible keys were split over several units: its candidates sit in the
+// store slots (unit u, query j) for u in [first_unit, first_unit + n_chunks) and are
+// merged into the slot `out_slot` before the selection.
+struct MergeDesc {
+  int32_t first_unit;
+  int32_t n_chunks;
+  int32_t j;         // query index within the units (0..3)
+  int32_t out_slot;  // store slot of the merged candidates
 };
 
 // Self-resetting work counter: CTAs draw items with atomicAdd on `next`; the last CTA to

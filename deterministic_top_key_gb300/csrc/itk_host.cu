@@ -41,11 +41,22 @@ int cuda_fail(cudaError_t e, const char* what) {
   return fail(ITK_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-// Validated copy of a descriptor plus its unit table.
+// Validated copy of a descriptor plus its work tables.
 struct Layout {
   int32_t T = 0, Tkv = 0, top_k = 0, B = 0;
-  std::vector<UnitDesc> units;  // ticket order: most key tiles first
+  std::vector<UnitDesc> units;     // ticket order: most key tiles first
+  std::vector<int32_t> item_rows;  // per store slot: output row, or -1 (empty or merged elsewhere)
+  std::vector<itk::MergeDesc> merges;
+  size_t n_slots() const { return item_rows.size(); }  // units * 4 + merges
 };
+
+// Split tails: a descriptor with at most kSplitMaxBlocks query blocks cannot fill the
+// GPU with one unit per block, so every block with at least 2 * kSplitTiles key tiles is
+// split into chunks of about kSplitTiles tiles (at most kSplitUnits units in all); the
+// chunks' candidates are merged per query before the selection.
+constexpr int kSplitMaxBlocks = 64;
+constexpr int kSplitTiles = 4;
+constexpr int kSplitUnits = 256;
 
 int build_layout(const itk_desc* d, Layout* out) {
   if (!d) return fail(ITK_ERR_INVALID_ARGUMENT, "descriptor is NULL");
@@ -80,7 +91,6 @@ int build_layout(const itk_desc* d, Layout* out) {
     struct Item {
       UnitDesc u;
       int64_t tiles;
-      int64_t order;
     };
     std::vector<Item> items;
     for (int b = 0; b < B; ++b) {
@@ -98,14 +108,44 @@ int build_layout(const itk_desc* d, Layout* out) {
         it.u.key_row0 = ck[b];
         it.u.pos0 = static_cast<int32_t>(off + i0);
         it.tiles = (int64_t(it.u.pos0) + it.u.nq + itk::kBlockKeys - 1) / itk::kBlockKeys;
-        it.order = static_cast<int64_t>(items.size());
+        it.u.tile0 = 0;
+        it.u.tile1 = static_cast<int32_t>(it.tiles);
         items.push_back(it);
       }
     }
     // Longest first: the heaviest units are handed out first so the short ones fill the tail.
     std::stable_sort(items.begin(), items.end(), [](const Item& a, const Item& b) { return a.tiles > b.tiles; });
-    L.units.reserve(items.size());
-    for (const Item& it : items) L.units.push_back(it.u);
+    const int64_t n_blocks = static_cast<int64_t>(items.size());
+    const int64_t chunk_budget = n_blocks > 0 ? std::max<int64_t>(1, kSplitUnits / n_blocks) : 1;
+    for (const Item& it : items) {
+      int64_t chunks = 1;
+      if (n_blocks <= kSplitMaxBlocks && it.tiles >= 2 * kSplitTiles)
+        chunks = std::min<int64_t>((it.tiles + kSplitTiles - 1) / kSplitTiles, chunk_budget);
+      const int32_t first = static_cast<int32_t>(L.units.size());
+      for (int64_t c = 0; c < chunks; ++c) {
+        UnitDesc u = it.u;
+        u.tile0 = static_cast<int32_t>(it.tiles * c / chunks);
+        u.tile1 = static_cast<int32_t>(it.tiles * (c + 1) / chunks);
+        L.units.push_back(u);
+        for (int j = 0; j < itk::kQB; ++j)
+          L.item_rows.push_back(chunks == 1 && j < u.nq ? u.q_row0 + j : -1);
+      }
+      if (chunks > 1)
+        for (int j = 0; j < it.u.nq; ++j) {
+          itk::MergeDesc m;
+          m.first_unit = first;
+          m.n_chunks = static_cast<int32_t>(chunks);
+          m.j = j;
+          m.out_slot = -1;  // set below, once the number of unit slots is known
+          L.merges.push_back(m);
+        }
+    }
+    const int32_t unit_slots = static_cast<int32_t>(L.units.size()) * itk::kQB;
+    for (size_t m = 0; m < L.merges.size(); ++m) {
+      L.merges[m].out_slot = unit_slots + static_cast<int32_t>(m);
+      const UnitDesc& u = L.units[L.merges[m].first_unit];
+      L.item_rows.push_back(u.q_row0 + L.merges[m].j);
+    }
   }
   *out = std::move(L);
   return ITK_OK;
@@ -174,32 +214,67 @@ int grid_for(size_t n_units, int sm_count) {
 }
 
 // Device block layout shared by the plan and the eager entry:
-// [units | scan ticket | selection ticket | status].
+// [units | item rows | merges | scan ticket | selection ticket | status].
 struct BlockLayout {
-  size_t units_off = 0, ticket_off = 0, sel_ticket_off = 0, status_off = 0, bytes = 0;
+  size_t units_off = 0, items_off = 0, merges_off = 0, ticket_off = 0, sel_ticket_off = 0, status_off = 0, bytes = 0;
 };
-BlockLayout block_layout(size_t n_units) {
+BlockLayout block_layout(const Layout& L) {
   BlockLayout b;
   b.units_off = 0;
-  b.ticket_off = align_up(n_units * sizeof(UnitDesc), 64);
+  b.items_off = align_up(L.units.size() * sizeof(UnitDesc), 64);
+  b.merges_off = align_up(b.items_off + L.item_rows.size() * sizeof(int32_t), 64);
+  b.ticket_off = align_up(b.merges_off + L.merges.size() * sizeof(itk::MergeDesc), 64);
   b.sel_ticket_off = b.ticket_off + sizeof(TicketBlock);
   b.status_off = b.sel_ticket_off + sizeof(TicketBlock);
   b.bytes = b.status_off + 16;
   return b;
 }
+// The block's initial contents: the tables, then zeroed ticket blocks and status word.
+std::vector<unsigned char> block_image(const Layout& L, const BlockLayout& b) {
+  std::vector<unsigned char> host(b.bytes, 0);
+  std::memcpy(host.data() + b.units_off, L.units.data(), L.units.size() * sizeof(UnitDesc));
+  std::memcpy(host.data() + b.items_off, L.item_rows.data(), L.item_rows.size() * sizeof(int32_t));
+  std::memcpy(host.data() + b.merges_off, L.merges.data(), L.merges.size() * sizeof(itk::MergeDesc));
+  return host;
+}
 
 // Workspace layout of one run: per-CTA working buffers of the scan, then the candidate
-// store (kCap keys per query slot, four slots per unit), then the per-slot counts.
+// store (kCap keys per slot: four slots per unit, then one per merged query), then the
+// per-slot counts.
 struct WorkLayout {
   size_t cand_off = 0, store_off = 0, counts_off = 0, bytes = 0;
 };
-constexpr WorkLayout work_layout(int grid, size_t n_units) {
+constexpr WorkLayout work_layout(int grid, size_t n_slots) {
   WorkLayout w;
   w.cand_off = 0;
   w.store_off = align_up(static_cast<size_t>(grid) * itk::candidate_bytes_per_cta(), 256);
-  w.counts_off = w.store_off + align_up(n_units * itk::store_bytes_per_unit(), 256);
-  w.bytes = w.counts_off + align_up(n_units * itk::kQB * sizeof(uint32_t), 256);
+  w.counts_off = w.store_off + align_up(n_slots * itk::kCap * sizeof(unsigned long long), 256);
+  w.bytes = w.counts_off + align_up(n_slots * sizeof(uint32_t), 256);
   return w;
+}
+
+// Device addresses of one run's tables.
+struct RunTables {
+  const UnitDesc* units = nullptr;
+  size_t n_units = 0;
+  const int32_t* item_rows = nullptr;
+  size_t n_slots = 0;
+  const itk::MergeDesc* merges = nullptr;
+  size_t n_merges = 0;
+  TicketBlock* tickets = nullptr;  // two adjacent blocks: scan, selection
+  uint32_t* status = nullptr;
+};
+RunTables block_tables(const Layout& L, const BlockLayout& b, char* blk) {
+  RunTables t;
+  t.units = reinterpret_cast<const UnitDesc*>(blk + b.units_off);
+  t.n_units = L.units.size();
+  t.item_rows = reinterpret_cast<const int32_t*>(blk + b.items_off);
+  t.n_slots = L.item_rows.size();
+  t.merges = reinterpret_cast<const itk::MergeDesc*>(blk + b.merges_off);
+  t.n_merges = L.merges.size();
+  t.tickets = reinterpret_cast<TicketBlock*>(blk + b.ticket_off);
+  t.status = reinterpret_cast<uint32_t*>(blk + b.status_off);
+  return t;
 }
 
 constexpr size_t kSelSmemLaunch = itk::kSelSmemBytes + 128;  // slack for 128-byte alignment
@@ -229,12 +304,12 @@ int check_run_buffers(const Layout& L, const void* q, const void* k, const float
   return ITK_OK;
 }
 
-// Encode maps and launch the scan over units [0, n_units) of d_units, then the selection
-// of the same units' queries. d_ticket points at two adjacent ticket blocks (scan,
-// selection); `work` is laid out by work_layout(grid, n_units).
-int launch_run(const Layout& L, int grid, int sm_count, const UnitDesc* d_units, size_t n_units, TicketBlock* d_ticket,
-               uint32_t* d_status, const void* q, const void* k, const float* w, int32_t* ids, float* scores,
-               void* work, cudaStream_t stream, bool force_launch_failure, cudaEvent_t split_event = nullptr) {
+// Encode maps and launch the scan over the units of `t`, the merge of split queries (if
+// any), then the selection of every slot with an output row. `work` is laid out by
+// work_layout(grid, t.n_slots).
+int launch_run(const Layout& L, int grid, int sm_count, const RunTables& t, const void* q, const void* k,
+               const float* w, int32_t* ids, float* scores, void* work, cudaStream_t stream,
+               bool force_launch_failure, cudaEvent_t split_event = nullptr) {
   CUtensorMap qmap, kmap;
   int rc = encode_rows(&qmap, q, static_cast<uint64_t>(L.T) * itk::kHeads, itk::kN);
   if (rc) return rc;
@@ -242,14 +317,14 @@ int launch_run(const Layout& L, int grid, int sm_count, const UnitDesc* d_units,
   if (rc) return rc;
   rc = ensure_kernel_attributes();
   if (rc) return rc;
-  const WorkLayout wl = work_layout(grid, n_units);
+  const WorkLayout wl = work_layout(grid, t.n_slots);
   char* wb = static_cast<char*>(work);
   itk::ScanParams prm;
-  prm.units = d_units;
-  prm.n_units = static_cast<int32_t>(n_units);
+  prm.units = t.units;
+  prm.n_units = static_cast<int32_t>(t.n_units);
   prm.top_k = L.top_k;
-  prm.ticket = d_ticket;
-  prm.status = d_status;
+  prm.ticket = t.tickets;
+  prm.status = t.status;
   prm.w = w;
   prm.cand = reinterpret_cast<unsigned long long*>(wb + wl.cand_off);
   prm.store = reinterpret_cast<unsigned long long*>(wb + wl.store_off);
@@ -264,17 +339,30 @@ int launch_run(const Layout& L, int grid, int sm_count, const UnitDesc* d_units,
     e = cudaEventRecord(split_event, stream);
     if (e != cudaSuccess) return cuda_fail(e, "recording the split event");
   }
+  if (t.n_merges > 0) {
+    itk::MergeParams mp;
+    mp.merges = t.merges;
+    mp.n_merges = static_cast<int32_t>(t.n_merges);
+    mp.top_k = L.top_k;
+    mp.units = t.units;
+    mp.store = prm.store;
+    mp.counts = prm.counts;
+    mp.status = t.status;
+    itk::indexer_topk_merge_kernel<<<static_cast<int>(t.n_merges), itk::kMergeThreads, 0, stream>>>(mp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  }
   itk::SelectParams sp;
-  sp.units = d_units;
-  sp.n_units = static_cast<int32_t>(n_units);
+  sp.item_rows = t.item_rows;
+  sp.n_items = static_cast<int32_t>(t.n_slots);
   sp.top_k = L.top_k;
-  sp.ticket = d_ticket + 1;
-  sp.status = d_status;
+  sp.ticket = t.tickets + 1;
+  sp.status = t.status;
   sp.store = prm.store;
   sp.counts = prm.counts;
   sp.out_ids = ids;
   sp.out_scores = scores;
-  const size_t items = n_units * itk::kQB;
+  const size_t items = t.n_slots;
   const int sel_grid = static_cast<int>(
       std::max<size_t>(1, std::min<size_t>(static_cast<size_t>(sm_count), (items + itk::kSelGroups - 1) / itk::kSelGroups)));
   itk::indexer_topk_select_kernel<<<sel_grid, itk::kSelThreads, kSelSmemLaunch, stream>>>(sp);
@@ -339,10 +427,12 @@ int64_t indexer_topk_unit_table(const itk_desc* desc, int32_t* units, int64_t ca
   if (units && capacity > 0) {
     const int64_t m = std::min(n, capacity);
     for (int64_t i = 0; i < m; ++i) {
-      units[4 * i + 0] = L.units[i].q_row0;
-      units[4 * i + 1] = L.units[i].nq;
-      units[4 * i + 2] = L.units[i].key_row0;
-      units[4 * i + 3] = L.units[i].pos0;
+      units[6 * i + 0] = L.units[i].q_row0;
+      units[6 * i + 1] = L.units[i].nq;
+      units[6 * i + 2] = L.units[i].key_row0;
+      units[6 * i + 3] = L.units[i].pos0;
+      units[6 * i + 4] = L.units[i].tile0;
+      units[6 * i + 5] = L.units[i].tile1;
     }
   }
   return n;
@@ -362,31 +452,28 @@ int indexer_topk_prepare(const itk_desc* desc, void* stream, itk_plan* out_plan)
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t n_units = plan->layout.units.size();
   plan->grid = grid_for(n_units, plan->dev.sm_count);
-  plan->bl = block_layout(n_units);
+  plan->bl = block_layout(plan->layout);
   cudaError_t e = cudaMalloc(&plan->block, plan->bl.bytes);
   if (e != cudaSuccess) {
     delete plan;
     return cuda_fail(e, "cudaMalloc of the plan block");
   }
-  char* blk = static_cast<char*>(plan->block);
-  if (n_units)
-    e = cudaMemcpyAsync(blk + plan->bl.units_off, plan->layout.units.data(), n_units * sizeof(UnitDesc),
-                        cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(blk + plan->bl.ticket_off, 0, plan->bl.bytes - plan->bl.ticket_off, s);
+  // Tables plus zeroed ticket blocks and status word in one copy. The runtime passes a
+  // pageable source through a staging buffer, so the image may be freed right away.
+  const std::vector<unsigned char> image = block_image(plan->layout, plan->bl);
+  e = cudaMemcpyAsync(plan->block, image.data(), image.size(), cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) {
     cudaFree(plan->block);
     delete plan;
     return cuda_fail(e, "uploading the plan block");
   }
-  // The host copy of the unit table is passed by the runtime through a staging buffer, so
-  // the vector may be read again or freed right away.
   *out_plan = plan;
   return ITK_OK;
 }
 
 size_t indexer_topk_workspace_bytes(itk_plan plan) {
   if (!plan) return 0;
-  return plan->grid > 0 ? work_layout(plan->grid, plan->layout.units.size()).bytes : 0;
+  return plan->grid > 0 ? work_layout(plan->grid, plan->layout.n_slots()).bytes : 0;
 }
 
 int indexer_topk_run(itk_plan plan, const void* q, const void* k, const float* w, int32_t* out_ids,
@@ -409,9 +496,8 @@ int indexer_topk_run(itk_plan plan, const void* q, const void* k, const float* w
   }
   const bool inject = plan->fail_next_launch;
   plan->fail_next_launch = false;
-  rc = launch_run(L, plan->grid, plan->dev.sm_count, reinterpret_cast<const UnitDesc*>(blk + plan->bl.units_off),
-                  L.units.size(), ticket, reinterpret_cast<uint32_t*>(blk + plan->bl.status_off), q, k, w, out_ids,
-                  out_scores, workspace, s, inject, plan->split_event);
+  rc = launch_run(L, plan->grid, plan->dev.sm_count, block_tables(L, plan->bl, blk), q, k, w, out_ids, out_scores,
+                  workspace, s, inject, plan->split_event);
   plan->ticket_dirty = (rc != ITK_OK);
   return rc;
 }
@@ -422,7 +508,7 @@ size_t indexer_topk_eager_workspace_bytes(const itk_desc* desc) {
   DeviceInfo dev;
   if (query_device(&dev)) return 0;
   const int grid = grid_for(L.units.size(), dev.sm_count);
-  return work_layout(grid, L.units.size()).bytes + block_layout(L.units.size()).bytes;
+  return work_layout(grid, L.n_slots()).bytes + block_layout(L).bytes;
 }
 
 int indexer_topk_eager(const itk_desc* desc, const void* q, const void* k, const float* w, int32_t* out_ids,
@@ -437,22 +523,19 @@ int indexer_topk_eager(const itk_desc* desc, const void* q, const void* k, const
   rc = check_run_buffers(L, q, k, w, out_ids, out_scores);
   if (rc) return rc;
   const int grid = grid_for(L.units.size(), dev.sm_count);
-  const size_t cand = work_layout(grid, L.units.size()).bytes;
-  const BlockLayout bl = block_layout(L.units.size());
+  const size_t cand = work_layout(grid, L.n_slots()).bytes;
+  const BlockLayout bl = block_layout(L);
   if (!workspace) return fail(ITK_ERR_NULL_POINTER, "workspace is NULL");
   if (workspace_bytes < cand + bl.bytes)
     return fail(ITK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, cand + bl.bytes);
   if (!aligned(workspace, 256)) return fail(ITK_ERR_MISALIGNED, "eager workspace must be 256-byte aligned");
-  // Unit table, zeroed ticket block and status word go up in one copy.
-  std::vector<unsigned char> host(bl.bytes, 0);
-  std::memcpy(host.data() + bl.units_off, L.units.data(), L.units.size() * sizeof(UnitDesc));
+  // Tables, zeroed ticket blocks and status word go up in one copy.
+  const std::vector<unsigned char> host = block_image(L, bl);
   char* blk = static_cast<char*>(workspace) + cand;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(blk, host.data(), bl.bytes, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "uploading the eager unit table");
-  return launch_run(L, grid, dev.sm_count, reinterpret_cast<const UnitDesc*>(blk + bl.units_off), L.units.size(),
-                    reinterpret_cast<TicketBlock*>(blk + bl.ticket_off),
-                    reinterpret_cast<uint32_t*>(blk + bl.status_off), q, k, w, out_ids, out_scores, workspace, s,
+  return launch_run(L, grid, dev.sm_count, block_tables(L, bl, blk), q, k, w, out_ids, out_scores, workspace, s,
                     false);
 }
 
@@ -524,9 +607,17 @@ namespace {
 constexpr int kNoAllocMaxCtas = 152;          // CTAs whose working buffers fit
 constexpr size_t kNoAllocChunkUnits = 512;    // work units per launch pair (2048 queries)
 constexpr int64_t kNoAllocMaxUnits = 65536;   // work units (4 queries each) the unit table holds
-constexpr size_t kNoAllocWorkBytes = work_layout(kNoAllocMaxCtas, kNoAllocChunkUnits).bytes;
+// Split queries (and so merges) exist only for descriptors of at most kSplitMaxBlocks
+// query blocks, whose at most kSplitUnits + kSplitMaxBlocks units fit one launch pair.
+constexpr size_t kNoAllocMaxMerges = static_cast<size_t>(kSplitMaxBlocks) * itk::kQB;
+static_assert(kSplitUnits + kSplitMaxBlocks <= static_cast<int>(kNoAllocChunkUnits), "split runs fit one chunk");
+constexpr size_t kNoAllocChunkSlots = kNoAllocChunkUnits * itk::kQB + kNoAllocMaxMerges;
+constexpr size_t kNoAllocWorkBytes = work_layout(kNoAllocMaxCtas, kNoAllocChunkSlots).bytes;
 constexpr size_t kNoAllocUnitsOff = kNoAllocWorkBytes;
-constexpr size_t kNoAllocTicketOff = kNoAllocUnitsOff + kNoAllocMaxUnits * sizeof(UnitDesc);
+constexpr size_t kNoAllocItemsOff = kNoAllocUnitsOff + align_up(kNoAllocMaxUnits * sizeof(UnitDesc), 256);
+constexpr size_t kNoAllocMergesOff =
+    kNoAllocItemsOff + align_up((kNoAllocMaxUnits * itk::kQB + kNoAllocMaxMerges) * sizeof(int32_t), 256);
+constexpr size_t kNoAllocTicketOff = kNoAllocMergesOff + align_up(kNoAllocMaxMerges * sizeof(itk::MergeDesc), 256);
 constexpr size_t kNoAllocStatusOff = kNoAllocTicketOff + 256;
 constexpr size_t kNoAllocBytes = kNoAllocStatusOff + 256;
 
@@ -576,23 +667,36 @@ int indexer_topk_run_noalloc(const itk_desc* desc, const void* q, const void* k,
   unsigned char* scratch = nullptr;
   rc = noalloc_scratch(dev.device, &scratch);
   if (rc) return rc;
-  // Unit table, then the ticket blocks and status word, which must start at zero: one
-  // copy and one memset on the call's stream (the array keeps the previous call's
+  // The tables, then the ticket blocks and status word, which must start at zero: three
+  // copies and one memset on the call's stream (the array keeps the previous call's
   // contents otherwise). Working buffers, store and counts need no clearing.
-  const size_t unit_bytes = L.units.size() * sizeof(UnitDesc);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(scratch + kNoAllocUnitsOff, L.units.data(), unit_bytes, cudaMemcpyHostToDevice, s);
+  cudaError_t e = cudaMemcpyAsync(scratch + kNoAllocUnitsOff, L.units.data(), L.units.size() * sizeof(UnitDesc),
+                                  cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(scratch + kNoAllocItemsOff, L.item_rows.data(), L.item_rows.size() * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && !L.merges.empty())
+    e = cudaMemcpyAsync(scratch + kNoAllocMergesOff, L.merges.data(), L.merges.size() * sizeof(itk::MergeDesc),
+                        cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(scratch + kNoAllocTicketOff, 0, kNoAllocBytes - kNoAllocTicketOff, s);
-  if (e != cudaSuccess) return cuda_fail(e, "staging the unit table into the static scratch");
-  const UnitDesc* d_units = reinterpret_cast<const UnitDesc*>(scratch + kNoAllocUnitsOff);
+  if (e != cudaSuccess) return cuda_fail(e, "staging the tables into the static scratch");
   for (size_t u0 = 0; u0 < L.units.size(); u0 += kNoAllocChunkUnits) {
     const size_t n = std::min(kNoAllocChunkUnits, L.units.size() - u0);
-    // work_layout(grid, n) of a chunk fits inside work_layout(kNoAllocMaxCtas, kNoAllocChunkUnits)
+    const bool whole = (u0 == 0 && n == L.units.size());  // merges only ever occur then
+    RunTables t;
+    t.units = reinterpret_cast<const UnitDesc*>(scratch + kNoAllocUnitsOff) + u0;
+    t.n_units = n;
+    t.item_rows = reinterpret_cast<const int32_t*>(scratch + kNoAllocItemsOff) + u0 * itk::kQB;
+    t.n_slots = n * itk::kQB + (whole ? L.merges.size() : 0);
+    t.merges = reinterpret_cast<const itk::MergeDesc*>(scratch + kNoAllocMergesOff);
+    t.n_merges = whole ? L.merges.size() : 0;
+    t.tickets = reinterpret_cast<TicketBlock*>(scratch + kNoAllocTicketOff);
+    t.status = reinterpret_cast<uint32_t*>(scratch + kNoAllocStatusOff);
+    // work_layout(grid, t.n_slots) of a chunk fits inside work_layout(kNoAllocMaxCtas, kNoAllocChunkSlots)
     const int grid = std::min(grid_for(n, dev.sm_count), kNoAllocMaxCtas);
-    rc = launch_run(L, grid, std::min(dev.sm_count, kNoAllocMaxCtas), d_units + u0, n,
-                    reinterpret_cast<TicketBlock*>(scratch + kNoAllocTicketOff),
-                    reinterpret_cast<uint32_t*>(scratch + kNoAllocStatusOff), q, k, w, out_ids, out_scores,
-                    scratch, s, false);
+    rc = launch_run(L, grid, std::min(dev.sm_count, kNoAllocMaxCtas), t, q, k, w, out_ids, out_scores, scratch, s,
+                    false);
     if (rc) return rc;
   }
   return ITK_OK;

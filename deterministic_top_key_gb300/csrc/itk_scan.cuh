@@ -113,9 +113,6 @@ struct Bars {
   __device__ uint32_t ue(int s) const { return unitempty + 8u * s; }
 };
 
-__device__ __forceinline__ int n_tiles_of(const int4& u) {
-  return (u.w + u.y + kBlockKeys - 1) / kBlockKeys;  // ceil((pos0 + nq) / 128)
-}
 
 // Two FP32 fused multiply-adds in one instruction: (d0, d1) = (a0*b0 + d0, a1*b1 + d1),
 // each rounded once, exactly as two fmaf calls.
@@ -392,15 +389,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           record_timeout(p.status, s_abort, 1);
           break;
         }
-        int4 unit;
+        int4 unit, range;
         if (u < static_cast<unsigned long long>(p.n_units)) {
           const UnitDesc d = p.units[u];
           unit = make_int4(d.q_row0, d.nq, d.key_row0, d.pos0);
+          range = make_int4(static_cast<int>(u), d.tile0, d.tile1, 0);
         } else {
           unit = make_int4(-1, 0, 0, 0);
+          range = make_int4(0, 0, 0, 0);
         }
         s_unit[2 * slot] = unit;
-        s_unit[2 * slot + 1] = make_int4(static_cast<int>(u), 0, 0, 0);
+        s_unit[2 * slot + 1] = range;  // unit index, key tiles [tile0, tile1)
         mbar_arrive(bars.uf(slot));
         if (unit.x < 0) break;
         if (!mbar_wait(bars.qempty, (it & 1) ^ 1, s_abort)) {
@@ -412,8 +411,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         tma_load_2d(qdst, &q_map, bars.qfull, 0, unit.x * kHeads, pol_q);
         tma_load_2d(qdst + kQHalfBytes, &q_map, bars.qfull, 64, unit.x * kHeads, pol_q);
         ++qloads;
-        const int nt = n_tiles_of(unit);
-        for (int tile = 0; tile < nt; ++tile, ++kc) {
+        for (int tile = range.y; tile < range.z; ++tile, ++kc) {
           const int s = kc % kStages;
           if (!mbar_wait(bars.ke(s), ((kc / kStages) & 1) ^ 1, s_abort)) {
             record_timeout(p.status, s_abort, 3);
@@ -454,7 +452,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           record_timeout(p.status, s_abort, 5);
           break;
         }
-        const int nt = n_tiles_of(unit);
+        const int nt = s_unit[2 * slot + 1].z - s_unit[2 * slot + 1].y;
         for (int tile = 0; tile < nt; ++tile, ++kc, ++ac) {
           const int ab = ac & 1;
           if (!mbar_wait(bars.ae(ab), ((ac >> 1) & 1) ^ 1, s_abort)) {
@@ -533,12 +531,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int4 unit = s_unit[2 * slot];
       if (unit.x < 0) break;
       const bool active = g < unit.y;  // uniform across the group
-      const size_t uidx = static_cast<size_t>(s_unit[2 * slot + 1].x);
+      const int4 range = s_unit[2 * slot + 1];
+      const size_t uidx = static_cast<size_t>(range.x);
       if (c.gtid < kHeads) s_w[g * kHeads + c.gtid] = active ? p.w[static_cast<size_t>(unit.x + g) * kHeads + c.gtid] : 0.f;
       for (int i = c.gtid; i < kBins / 2; i += 128) hist_g[i] = 0u;
       if (c.gtid < 4) qs[c.gtid] = 0u;
       gsync(c);
-      const int nt = n_tiles_of(unit);
+      const int tile0 = range.y, nt = range.z - range.y;
       const int last_key = unit.w + g;  // causal bound: local keys 0..last_key are visible
       bool failed = false;
       uint32_t thr = 0u;  // threshold bin, refreshed at every sync point
@@ -567,7 +566,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           continue;
         }
         tc_fence_after_sync();
-        const int jl = tile * kBlockKeys + key_lane;  // local key index within the segment
+        const int jl = (tile0 + tile) * kBlockKeys + key_lane;  // local key index within the segment
         uint32_t key32 = 0u;
         if (active) {
           const uint32_t col = static_cast<uint32_t>(ab * kN + g * kHeads);

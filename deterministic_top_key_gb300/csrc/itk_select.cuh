@@ -50,13 +50,13 @@ __device__ __forceinline__ uint32_t bin_pad(uint32_t b) { return b + (b >> 4); }
 __device__ __forceinline__ uint32_t sub_pad(uint32_t i) { return i + (i >> 5); }
 
 struct SelectParams {
-  const UnitDesc* units;              // the scan's unit table; item i is query i % 4 of unit i / 4
-  int32_t n_units;
+  const int32_t* item_rows;           // per store slot: output row, or -1 (nothing to select there)
+  int32_t n_items;                    // store slots
   int32_t top_k;
   TicketBlock* ticket;
   uint32_t* status;
-  const unsigned long long* store;    // [n_units * 4][kCap] candidate keys
-  const uint32_t* counts;             // [n_units * 4] candidates per item
+  const unsigned long long* store;    // [n_items][kCap] candidate keys
+  const uint32_t* counts;             // [n_items] candidates per slot
   int32_t* out_ids;                   // [T, top_k]
   float* out_scores;                  // [T, top_k]
 };
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) indexer_topk_select_kernel(con
   unsigned long long* stage = reinterpret_cast<unsigned long long*>(gs + kSgStage);
   uint32_t* flags = reinterpret_cast<uint32_t*>(gs + kSgFlags);
   volatile unsigned long long* s_item = reinterpret_cast<volatile unsigned long long*>(gs + kSgItem);
-  const unsigned long long n_items = static_cast<unsigned long long>(p.n_units) * kQB;
+  const unsigned long long n_items = static_cast<unsigned long long>(p.n_items);
 
   while (true) {
     if (c.gtid == 0) *s_item = atomicAdd(&p.ticket->next, 1ull);
@@ -311,10 +311,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) indexer_topk_select_kernel(con
     const unsigned long long item = *s_item;
     gsync(c);  // every thread has read the item before the next draw overwrites it
     if (item >= n_items) break;
-    const UnitDesc u = p.units[item / kQB];
-    const int j = static_cast<int>(item % kQB);
-    if (j >= u.nq) continue;
-    const size_t row = static_cast<size_t>(u.q_row0 + j);
+    const int32_t out_row = p.item_rows[item];
+    if (out_row < 0) continue;
+    const size_t row = static_cast<size_t>(out_row);
     uint32_t n = p.counts[item];
     if (n > static_cast<uint32_t>(kCap)) {  // cannot happen: the scan hands off at most kCap keys
       if (c.gtid == 0) atomicOr(p.status, kStatusInternal | (20u << 8));
@@ -327,4 +326,143 @@ __global__ void __launch_bounds__(kSelThreads, 1) indexer_topk_select_kernel(con
   if (threadIdx.x == 0) ticket_release(p.ticket);
 }
 
+// ------------------------------------------------------------------ split-query merge
+// A query whose visible keys were scanned by several units (a split tail) has one
+// candidate list per unit. One 256-thread CTA per such query histograms the union over
+// the 2048 score bins, keeps every key in the bins that reach the first top_k positions
+// when that fits in kCap, and otherwise keeps exactly the top_k keys (a radix select on
+// the bits below the bin inside the crossing bin). The result goes to the query's own
+// store slot, which the selection kernel then sorts like any other.
+constexpr int kMergeThreads = 256;
+
+struct MergeParams {
+  const MergeDesc* merges;
+  int32_t n_merges;
+  int32_t top_k;
+  const UnitDesc* units;
+  unsigned long long* store;
+  uint32_t* counts;
+  uint32_t* status;
+};
+
+__global__ void __launch_bounds__(kMergeThreads) indexer_topk_merge_kernel(const MergeParams p) {
+  __shared__ uint32_t hist[kBins];
+  __shared__ uint32_t radix[256];
+  __shared__ uint32_t sel[8];
+  __shared__ uint32_t wsum[kMergeThreads / 32];
+  __shared__ uint32_t s_cursor;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const MergeDesc m = p.merges[blockIdx.x];
+  const uint32_t K = static_cast<uint32_t>(p.top_k);
+  GroupCtx c;  // warp 0 picks radix digits, as in a 128-thread group
+  c.gtid = tid;
+  c.gwarp = warp;
+  c.lane = lane;
+  c.bar = 0;
+  c.radix = radix;
+  c.sel = sel;
+  auto chunk_slot = [&](int ch) { return static_cast<size_t>(m.first_unit + ch) * kQB + m.j; };
+  auto chunk_count = [&](int ch) {
+    const uint32_t n = p.counts[chunk_slot(ch)];
+    return n < static_cast<uint32_t>(kCap) ? n : static_cast<uint32_t>(kCap);
+  };
+  for (int i = tid; i < kBins; i += kMergeThreads) hist[i] = 0u;
+  __syncthreads();
+  for (int ch = 0; ch < m.n_chunks; ++ch) {
+    const unsigned long long* src = p.store + chunk_slot(ch) * kCap;
+    const uint32_t n = chunk_count(ch);
+    for (uint32_t i = tid; i < n; i += kMergeThreads) atomicAdd(&hist[bin_of(src[i])], 1u);
+  }
+  __syncthreads();
+  // ge(b) = keys in bins >= b: each thread sums 8 bins, highest bins first
+  constexpr int kPer = kBins / kMergeThreads;
+  uint32_t loc[kPer];
+  uint32_t s = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    loc[i] = hist[kBins - 1 - (kPer * tid + i)];
+    s += loc[i];
+  }
+  uint32_t incl = s;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  if (tid == 0) sel[3] = 0u;  // tstar: the lowest bin kept (0 when fewer than K keys in all)
+  __syncthreads();
+  uint32_t run = incl - s;
+  for (int wv = 0; wv < warp; ++wv) run += wsum[wv];
+  __syncthreads();  // every thread has its run before hist is rewritten
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const uint32_t b = kBins - 1 - (kPer * tid + i);
+    const uint32_t above = run;  // keys in bins > b
+    run += loc[i];
+    hist[b] = run;               // now ge(b)
+    if (above < K && run >= K) sel[3] = b;  // the bin that reaches position K (at most one)
+  }
+  __syncthreads();
+  const uint32_t tstar = sel[3];
+  const uint32_t ge_t = hist[tstar];
+  const uint32_t ge_above = tstar + 1 < static_cast<uint32_t>(kBins) ? hist[tstar + 1] : 0u;
+  __syncthreads();
+  unsigned long long thr_key = static_cast<unsigned long long>(tstar) << (32 + kBinShift);
+  if (ge_t > static_cast<uint32_t>(kCap)) {
+    // exactly K: keys above bin tstar plus the (K - ge_above) largest inside bin tstar,
+    // found by a radix select on the 53 bits below the bin (shifted to the top)
+    unsigned long long prefix = 0ull;
+    uint32_t k_rem = K - ge_above;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += kMergeThreads) radix[i] = 0u;
+      __syncthreads();
+      const unsigned long long hi_mask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
+      for (int ch = 0; ch < m.n_chunks; ++ch) {
+        const unsigned long long* src = p.store + chunk_slot(ch) * kCap;
+        const uint32_t n = chunk_count(ch);
+        for (uint32_t i = tid; i < n; i += kMergeThreads) {
+          const unsigned long long x = src[i];
+          const unsigned long long y = x << (32 - kBinShift);  // the bits below the bin
+          if (bin_of(x) == tstar && (y & hi_mask) == (prefix & hi_mask)) atomicAdd(&radix[(y >> shift) & 0xFFu], 1u);
+        }
+      }
+      __syncthreads();
+      group_pick_digit(c, k_rem);
+      __syncthreads();
+      prefix |= static_cast<unsigned long long>(sel[0]) << shift;
+      k_rem = sel[1];
+      const uint32_t cnt = sel[2];
+      __syncthreads();
+      if (cnt == k_rem) break;  // uniform
+    }
+    thr_key |= prefix >> (32 - kBinShift);
+  }
+  // keep every key at or above the threshold key
+  if (tid == 0) s_cursor = 0u;
+  __syncthreads();
+  unsigned long long* dst = p.store + static_cast<size_t>(m.out_slot) * kCap;
+  for (int ch = 0; ch < m.n_chunks; ++ch) {
+    const unsigned long long* src = p.store + chunk_slot(ch) * kCap;
+    const uint32_t n = chunk_count(ch);
+    for (uint32_t base = 0; base < n; base += kMergeThreads) {
+      const uint32_t i = base + tid;
+      const unsigned long long x = i < n ? src[i] : 0ull;
+      const bool keep = i < n && x >= thr_key;
+      const uint32_t slot = warp_append_slot(keep, &s_cursor, lane);
+      if (keep && slot < static_cast<uint32_t>(kCap)) dst[slot] = x;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t n = s_cursor;
+    if (n > static_cast<uint32_t>(kCap)) {  // cannot happen: at most max(ge_t, K) <= kCap keys qualify
+      atomicOr(p.status, kStatusInternal | (22u << 8));
+      n = kCap;
+    }
+    p.counts[m.out_slot] = n;
+  }
+}
+
 }  // namespace itk
+

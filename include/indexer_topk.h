@@ -109,10 +109,11 @@ ITK_API int indexer_topk_prepare(const itk_desc* desc, void* stream, itk_plan* o
 ITK_API size_t indexer_topk_workspace_bytes(itk_plan plan);
 
 /*
- * One scan on `stream`: exactly two kernel launches -- the scan, which leaves each
- * query's candidates (a superset of its top-k, at most 4096 keys) in the workspace, then
- * the selection, which writes the sorted top-k rows -- plus a 32-byte memset only right
- * after a failed launch. Arguments:
+ * One scan on `stream`: two kernel launches -- the scan, which leaves each query's
+ * candidates (a superset of its top-k, at most 4096 keys) in the workspace, then the
+ * selection, which writes the sorted top-k rows -- with a third launch between them, the
+ * merge of split queries, for split-tail descriptors (see indexer_topk_unit_table); plus a
+ * 32-byte memset only right after a failed launch. Arguments:
  *   q          device, BF16 [T,H,D] row-major, 16-byte aligned
  *   k          device, BF16 [Tkv,D] row-major, 16-byte aligned
  *   w          device, FP32 [T,H] row-major
@@ -162,10 +163,16 @@ ITK_API int indexer_topk_validate(const itk_desc* desc);
 ITK_API int64_t indexer_topk_num_units(const itk_desc* desc);
 
 /*
- * Host-only view of the work-unit table, in ticket order (longest first): for each unit
- * {first query row, number of queries (1..4), first key row of the segment, causal
- * position of the first query}. Writes min(capacity, n) units to `units` (int32
- * [capacity][4]) and returns n, or -status on an invalid descriptor.
+ * Host-only view of the work-unit table, in ticket order (longest query block first): for
+ * each unit {first query row, number of queries (1..4), first key row of the segment,
+ * causal position of the first query, first key tile, end key tile} -- the unit scans key
+ * tiles [first, end) of 128 keys. A descriptor with at most 64 query blocks (a "split
+ * tail") has every block of at least 8 visible key tiles split into consecutive units of
+ * about 4 tiles (at most 256 units in all), whose candidates are merged per query before
+ * the selection; otherwise a unit covers all visible tiles of its block. Writes min(capacity, n)
+ * units to `units` (int32 [capacity][6]) and returns n, or -status on an invalid
+ * descriptor. Reference: flashinfer PR #8691, benchmark rows A1-A3 ("split tail: 4
+ * queries in one segment").
  */
 ITK_API int64_t indexer_topk_unit_table(const itk_desc* desc, int32_t* units, int64_t capacity);
 

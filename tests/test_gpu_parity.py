@@ -155,3 +155,27 @@ def test_eager_matches_prepared(binding, dev):
     torch.cuda.synchronize()
     np.testing.assert_array_equal(ids1.cpu().numpy(), ids0)
     np.testing.assert_array_equal(sc1.cpu().numpy().view(np.uint32), sc0.view(np.uint32))
+
+
+@pytest.mark.parametrize("kind", ["normal", "int"])
+def test_split_tail_matches_unsplit(binding, dev, oracle_mod, kind):
+    """Four queries over 5000 keys form a split tail (10 units of about 4 key tiles,
+    merged per query); the same four queries inside a descriptor of 66 query blocks run
+    as one unit. Rows are bit-identical, and equal to the oracle on integer inputs."""
+    tq, tk = [4, 260], [5000, 300]
+    cu_q = np.concatenate([[0], np.cumsum(tq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(tk)]).astype(np.int32)
+    big = inputs.draw(int(cu_q[-1]), int(cu_k[-1]), cu_q, cu_k, 2048, seed=21, kind=kind)
+    assert len(binding.indexer_topk_unit_table(binding.Desc(big.T, big.Tkv, cu_q, cu_k, 2048))) == 66
+    small = inputs.Workload("split", big.q_bits[:4], big.k_bits[:5000], big.w[:4], np.array([0, 4], np.int32),
+                            np.array([0, 5000], np.int32), None, 2048)
+    assert len(binding.indexer_topk_unit_table(binding.Desc(4, 5000, [0, 4], [0, 5000], 2048))) == 10
+    ids_b, sc_b = run_plan(binding, big, dev)
+    ids_s, sc_s = run_plan(binding, small, dev)
+    np.testing.assert_array_equal(ids_s, ids_b[:4])
+    np.testing.assert_array_equal(sc_s.view(np.uint32), sc_b[:4].view(np.uint32))
+    if kind == "int":
+        r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(small))
+        parity.assert_exact(ids_s, sc_s, r_ids, r_sc)
+    else:
+        parity.assert_close(ids_s, sc_s, small, np.arange(4))
