@@ -273,11 +273,16 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=20.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--residency", action="store_true",
+                    help="instead of the standard line: time the call while a kernel on another stream holds 1 or "
+                         "32 SMs, with the ticket schedule and with a fixed schedule")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.residency:
+        return run_residency(args)
     return run_ours(args)
 
 
@@ -331,6 +336,62 @@ def _step_ms(starts, splits, ends):
     scan = np.array([a.elapsed_time(b) for a, b in zip(starts, splits)])
     sel = np.array([a.elapsed_time(b) for a, b in zip(splits, ends)])
     return float(total.mean()), float(scan.mean()), float(sel.mean())
+
+
+def run_residency(args):
+    """Side-stream residency benchmark (flashinfer PR #8691, opening description and the
+    side-stream table): a kernel on a second stream holds n SMs (so that n scan CTAs cannot
+    start) for about one call's time, launched just before each call. With the ticket
+    schedule the running CTAs take every unit and the held CTAs find none left; with a
+    fixed schedule (CTA b owns units b, b + grid, ...) the held CTAs' units run as a second
+    wave after the holder leaves. Prints one JSON line of per-call times and ratios."""
+    import torch
+
+    from deterministic_top_key_gb300 import binding, inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    binding.load()
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2_bytes, 256 << 20), dtype=torch.uint8, device=dev)
+    wl = inputs.make(args.config)
+    plan, bufs, stream = _measure(binding, torch, wl, dev, args.steps, args.warmup, flush_buf)
+    side = torch.cuda.Stream()
+
+    def timed(hold_sms, hold_us, static):
+        binding.indexer_topk_debug_inject(plan, 3 if static else 4)
+        ms = []
+        for i in range(args.warmup + args.steps):
+            flush_buf.fill_(i & 0xFF)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            binding.indexer_topk_bench_hold(hold_sms, hold_us, side)
+            a.record(stream)
+            binding.indexer_topk_run(plan, *bufs, stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                ms.append(a.elapsed_time(b))
+        binding.indexer_topk_debug_inject(plan, 4)
+        plan.device_status()
+        return float(np.median(ms))
+
+    base = timed(0, 0, False)
+    base_static = timed(0, 0, True)
+    hold_us = int(base * 1000)
+    rows = {}
+    for n in (1, 32):
+        t_ticket = timed(n, hold_us, False)
+        t_static = timed(n, hold_us, True)
+        rows[f"hold_{n}"] = {"ticket_ms": t_ticket, "fixed_ms": t_static, "ticket_ratio": t_ticket / base,
+                             "fixed_ratio": t_static / base_static}
+    plan.destroy()
+    line = {"metric": "call time with n SMs held by another stream, relative to none held", "unit": "ratio",
+            "config": {"workload": f"{wl.name}: {inputs.config(wl.name)['desc']}", "hold_us": hold_us},
+            "base_ms": {"ticket": base, "fixed": base_static}, "rows": rows, "steps": args.steps,
+            "warmup": args.warmup, "data": "synthetic"}
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 def run_ours(args):

@@ -85,6 +85,7 @@ def load():
         "indexer_topk_run_noalloc": (ctypes.c_int, [DP, vp, vp, vp, vp, vp, vp]),
         "indexer_topk_noalloc_scratch_bytes": (sz, []),
         "indexer_topk_set_split_event": (ctypes.c_int, [vp, vp]),
+        "indexer_topk_bench_hold": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -224,6 +225,11 @@ def indexer_topk_set_split_event(plan: Plan, event=None):
     stops it."""
     handle = None if event is None else (event.cuda_event if hasattr(event, "cuda_event") else int(event))
     _check(load().indexer_topk_set_split_event(plan.handle, handle))
+
+
+def indexer_topk_bench_hold(n_ctas: int, microseconds: int, stream=None):
+    """Keep n_ctas SMs busy for `microseconds` with a kernel on `stream` (benchmark aid)."""
+    _check(load().indexer_topk_bench_hold(int(n_ctas), int(microseconds), _stream_handle(stream)))
 
 
 def indexer_topk_debug_inject(plan: Plan, what: int, stream=None):

@@ -309,7 +309,7 @@ int check_run_buffers(const Layout& L, const void* q, const void* k, const float
 // work_layout(grid, t.n_slots).
 int launch_run(const Layout& L, int grid, int sm_count, const RunTables& t, const void* q, const void* k,
                const float* w, int32_t* ids, float* scores, void* work, cudaStream_t stream,
-               bool force_launch_failure, cudaEvent_t split_event = nullptr) {
+               bool force_launch_failure, cudaEvent_t split_event = nullptr, bool static_schedule = false) {
   CUtensorMap qmap, kmap;
   int rc = encode_rows(&qmap, q, static_cast<uint64_t>(L.T) * itk::kHeads, itk::kN);
   if (rc) return rc;
@@ -329,6 +329,7 @@ int launch_run(const Layout& L, int grid, int sm_count, const RunTables& t, cons
   prm.cand = reinterpret_cast<unsigned long long*>(wb + wl.cand_off);
   prm.store = reinterpret_cast<unsigned long long*>(wb + wl.store_off);
   prm.counts = reinterpret_cast<uint32_t*>(wb + wl.counts_off);
+  prm.static_schedule = static_schedule ? 1 : 0;
   // A test hook asks for a launch the runtime must refuse: a dynamic shared-memory request
   // above the device limit is rejected at launch time and no work reaches the GPU.
   const size_t smem = force_launch_failure ? size_t(1) << 30 : itk::kSmemBytes;
@@ -382,6 +383,7 @@ struct itk_plan_s {
   bool ticket_dirty = false;
   bool fail_next_launch = false;  // test hook
   cudaEvent_t split_event = nullptr;  // recorded between the two launches when set
+  bool static_schedule = false;       // benchmark aid (debug_inject 3 / 4)
 };
 
 extern "C" {
@@ -497,7 +499,7 @@ int indexer_topk_run(itk_plan plan, const void* q, const void* k, const float* w
   const bool inject = plan->fail_next_launch;
   plan->fail_next_launch = false;
   rc = launch_run(L, plan->grid, plan->dev.sm_count, block_tables(L, plan->bl, blk), q, k, w, out_ids, out_scores,
-                  workspace, s, inject, plan->split_event);
+                  workspace, s, inject, plan->split_event, plan->static_schedule);
   plan->ticket_dirty = (rc != ITK_OK);
   return rc;
 }
@@ -587,10 +589,56 @@ int indexer_topk_debug_inject(itk_plan plan, int what, void* stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? ITK_OK : cuda_fail(e, "poisoning the ticket block");
   }
+  if (what == 3 || what == 4) {
+    plan->static_schedule = (what == 3);
+    return ITK_OK;
+  }
   return fail(ITK_ERR_INVALID_ARGUMENT, "unknown injection %d", what);
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- residency holder
+// Benchmark aid, not part of the operation: a kernel that keeps n SMs busy, as a kernel
+// of another stream would, to show that the scan's ticket grid does not run a second wave
+// of work units when some of its CTAs cannot start (flashinfer PR #8691, the side-stream
+// table and its opening description, issue #7548). Each holder CTA claims enough shared
+// memory that no scan CTA fits beside it, then sleeps in a clock-limited loop.
+namespace {
+
+constexpr size_t kHoldSmem = 128 * 1024;
+constexpr long long kHoldMaxCycles = 200000000ll;  // about 0.1 s at 2 GHz, whatever is asked
+
+__global__ void itk_hold_kernel(long long cycles) {
+  extern __shared__ uint8_t hold_smem[];
+  if (threadIdx.x == 0) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < cycles) __nanosleep(2000);
+    hold_smem[0] = 1;
+  }
+}
+
+}  // namespace
+
+extern "C" int indexer_topk_bench_hold(int n_ctas, int microseconds, void* stream) {
+  if (n_ctas < 0 || microseconds < 0) return fail(ITK_ERR_INVALID_ARGUMENT, "negative holder size or time");
+  if (n_ctas == 0 || microseconds == 0) return ITK_OK;
+  int dev = 0, khz = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the SM clock rate");
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(itk_hold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(kHoldSmem));
+  });
+  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute (holder)");
+  const long long cycles = std::min<long long>(static_cast<long long>(microseconds) * khz / 1000, kHoldMaxCycles);
+  itk_hold_kernel<<<n_ctas, 32, kHoldSmem, static_cast<cudaStream_t>(stream)>>>(cycles);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? ITK_OK : cuda_fail(e, "holder launch");
+}
 
 // ---------------------------------------------------------------- no-allocation entry
 // For callers that cannot allocate device memory at call time: a serving runtime or a

@@ -93,7 +93,8 @@ struct ScanParams {
   const float* w;                // [T,64]
   unsigned long long* cand;      // per CTA: 4 x kQCap working keys, then 4 x kMaxTopK exact-select scratch
   unsigned long long* store;     // [n_units * 4][kCap] candidate keys handed to the selection kernel
-  uint32_t* counts;              // [n_units * 4] keys in each store slot
+  uint32_t* counts;              // [n_slots] keys in each store slot
+  int32_t static_schedule;       // benchmark aid: 1 = CTA b takes units b, b + grid, ... (no ticket)
 };
 
 constexpr size_t kCandKeysPerCta = static_cast<size_t>(kQB) * kQCap + kEpiGroups * kMaxTopK;
@@ -383,7 +384,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       uint32_t it = 0, kc = 0, qloads = 0;
       bool ok = true;
       while (ok) {
-        const unsigned long long u = atomicAdd(&p.ticket->next, 1ull);
+        const unsigned long long u = p.static_schedule
+                                         ? static_cast<unsigned long long>(blockIdx.x) + it * gridDim.x
+                                         : atomicAdd(&p.ticket->next, 1ull);
         const int slot = it & 1;
         if (!mbar_wait(bars.ue(slot), ((it >> 1) & 1) ^ 1, s_abort)) {
           record_timeout(p.status, s_abort, 1);

@@ -218,16 +218,30 @@ ITK_API int indexer_topk_run_noalloc(const itk_desc* desc, const void* q, const 
  */
 ITK_API int indexer_topk_set_split_event(itk_plan plan, void* event);
 
+/*
+ * Benchmark aid, not part of the operation: launch on `stream` a kernel of n_ctas CTAs
+ * that each claim 128 KB of shared memory (so no scan CTA fits on the same SM) and stay
+ * resident for `microseconds` (capped at about 0.1 s), the way a kernel of another
+ * stream holds SMs. Used to show that the ticket grid runs no second wave of work units
+ * when some of its CTAs cannot start (flashinfer PR #8691, opening description and the
+ * side-stream table). 0 CTAs or 0 us launch nothing.
+ */
+ITK_API int indexer_topk_bench_hold(int n_ctas, int microseconds, void* stream);
+
 /* Size in bytes of the static scratch array used by indexer_topk_run_noalloc. */
 ITK_API size_t indexer_topk_noalloc_scratch_bytes(void);
 
 /*
- * Test hook for the host-side recovery tests; not part of the operation.
+ * Test and benchmark hook; not part of the operation.
  *   what = 1: the next indexer_topk_run's launch is refused by the CUDA runtime (an
  *             oversized shared-memory request; no work reaches the GPU), as after a run
  *             that raised while launching. The run returns ITK_ERR_CUDA.
- *   what = 2: write a nonzero pattern into the plan's ticket block on `stream` and wait
- *             for it, as a scan that stopped midway would leave the block.
+ *   what = 2: write a nonzero pattern into the plan's ticket blocks on `stream` and wait
+ *             for it, as a scan that stopped midway would leave them.
+ *   what = 3: later runs of the plan give scan CTA b the fixed units b, b + grid, ...
+ *             instead of drawing them from the ticket word (the schedule the ticket
+ *             replaces; results are the same, but a CTA that cannot start delays its
+ *             units). what = 4 restores the ticket.
  */
 ITK_API int indexer_topk_debug_inject(itk_plan plan, int what, void* stream);
 

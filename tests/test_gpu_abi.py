@@ -151,3 +151,23 @@ def test_cuda_graph_capture_and_replay(env):
     plan.device_status()
     del g
     plan.destroy()
+
+
+def test_runs_correct_while_sms_are_held(env):
+    """A kernel of another stream holds 32 SMs while the scan runs, with the ticket schedule
+    and with the fixed one: the call completes and every row stays exact."""
+    binding, torch, dev, wl, (q, k, w), (r_ids, r_sc) = env
+    plan = binding.indexer_topk_prepare(wl.T, wl.Tkv, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.top_k)
+    ws = torch.empty(plan.workspace_bytes(), dtype=torch.uint8, device=dev)
+    ids, sc = _bufs(torch, dev, wl)
+    side = torch.cuda.Stream()
+    for what in (4, 3, 4):  # ticket, fixed, ticket again
+        binding.indexer_topk_debug_inject(plan, what)
+        ids.fill_(5)
+        torch.cuda.synchronize()
+        binding.indexer_topk_bench_hold(32, 2000, side)
+        binding.indexer_topk_run(plan, q, k, w, ids, sc, ws)
+        torch.cuda.synchronize()
+        parity.assert_exact(ids.cpu().numpy(), sc.cpu().numpy(), r_ids, r_sc)
+    plan.device_status()
+    plan.destroy()
