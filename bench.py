@@ -338,6 +338,91 @@ def _step_ms(starts, splits, ends):
     return float(total.mean()), float(scan.mean()), float(sel.mean())
 
 
+def _e2e(binding, torch, wl, plan, bufs, stream, args, flush_buf, flops, world, dist, dev):
+    """End to end through the public API: every step copies its inputs from pinned host
+    memory, runs the scan and copies the ids and scores back to pinned host memory.
+
+    Two measurements. `serial`: copy in, run, copy out, one after another on one stream.
+    `value` (pipelined): the way a serving loop would overlap them: the copy-in of step
+    i + 1 and the copy-out of step i - 1 run on their own streams while step i computes
+    (double-buffered device inputs and outputs); the timed region spans the first copy-in
+    to the last copy-out, so it holds every step's copies."""
+    q, k, w, ids, sc, ws = bufs
+    hq = torch.from_numpy(wl.q_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hk = torch.from_numpy(wl.k_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hw = torch.from_numpy(wl.w).pin_memory()
+    hid = [torch.empty(ids.shape, dtype=torch.int32).pin_memory() for _ in range(2)]
+    hsc = [torch.empty(sc.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    h2d = hq.numel() * 2 + hk.numel() * 2 + hw.numel() * 4
+    d2h = hid[0].numel() * 4 + hsc[0].numel() * 4
+
+    # serial: one stream, steps back to back
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.warmup + args.steps):
+        flush_buf.fill_(i & 0xFF)
+        if i >= args.warmup:
+            e_s[i - args.warmup].record(stream)
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        w.copy_(hw, non_blocking=True)
+        binding.indexer_topk_run(plan, q, k, w, ids, sc, ws, stream)
+        hid[0].copy_(ids, non_blocking=True)
+        hsc[0].copy_(sc, non_blocking=True)
+        if i >= args.warmup:
+            e_e[i - args.warmup].record(stream)
+    torch.cuda.synchronize()
+    serial_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in zip(e_s, e_e)])), dist, dev)
+
+    # pipelined: copy-in stream, compute stream, copy-out stream, two buffer sets
+    dq = [q, torch.empty_like(q)]
+    dk = [k, torch.empty_like(k)]
+    dw = [w, torch.empty_like(w)]
+    did = [ids, torch.empty_like(ids)]
+    dsc = [sc, torch.empty_like(sc)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    loaded = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    drained = [torch.cuda.Event() for _ in range(2)]
+
+    def pipeline(n_steps, t0=None, t1=None):
+        for i in range(n_steps):
+            b = i & 1
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(computed[b])  # step i - 2 has read this input set
+                if i == 0 and t0 is not None:
+                    t0.record(s_in)
+                dq[b].copy_(hq, non_blocking=True)
+                dk[b].copy_(hk, non_blocking=True)
+                dw[b].copy_(hw, non_blocking=True)
+                loaded[b].record(s_in)
+            stream.wait_event(loaded[b])
+            if i >= 2:
+                stream.wait_event(drained[b])  # step i - 2's outputs are on the host
+            binding.indexer_topk_run(plan, dq[b], dk[b], dw[b], did[b], dsc[b], ws, stream)
+            computed[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(computed[b])
+                hid[b].copy_(did[b], non_blocking=True)
+                hsc[b].copy_(dsc[b], non_blocking=True)
+                drained[b].record(s_out)
+        if t1 is not None:
+            t1.record(s_out)
+
+    torch.cuda.synchronize()
+    pipeline(args.warmup)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pipeline(args.steps, t0, t1)
+    torch.cuda.synchronize()
+    pipe_ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, dist, dev)
+    return {"value": job_tflops(flops, world, pipe_ms), "unit": "TFLOP/s", "ms_per_step": pipe_ms,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "pipelined": True, "serial": {"value": job_tflops(flops, world, serial_ms), "ms_per_step": serial_ms},
+            "note": "copies of step i + 1 (in) and i - 1 (out) overlap step i's compute; serial = no overlap"}
+
+
 def run_residency(args):
     """Side-stream residency benchmark (flashinfer PR #8691, opening description and the
     side-stream table): a kernel on a second stream holds n SMs (so that n scan CTAs cannot
@@ -442,31 +527,7 @@ def run_ours(args):
     # end to end through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
-        hq = torch.from_numpy(wl.q_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-        hk = torch.from_numpy(wl.k_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-        hw = torch.from_numpy(wl.w).pin_memory()
-        hid = torch.empty(ids.shape, dtype=torch.int32).pin_memory()
-        hsc = torch.empty(sc.shape, dtype=torch.float32).pin_memory()
-        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        for i in range(args.warmup + args.steps):
-            flush_buf.fill_(i & 0xFF)
-            if i >= args.warmup:
-                e_s[i - args.warmup].record(stream)
-            q.copy_(hq, non_blocking=True)
-            k.copy_(hk, non_blocking=True)
-            w.copy_(hw, non_blocking=True)
-            binding.indexer_topk_run(plan, q, k, w, ids, sc, ws, stream)
-            hid.copy_(ids, non_blocking=True)
-            hsc.copy_(sc, non_blocking=True)
-            if i >= args.warmup:
-                e_e[i - args.warmup].record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(e_s, e_e)])), dist, dev)
-        h2d = hq.numel() * 2 + hk.numel() * 2 + hw.numel() * 4
-        d2h = hid.numel() * 4 + hsc.numel() * 4
-        e2e = {"value": job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        e2e = _e2e(binding, torch, wl, plan, bufs, stream, args, flush_buf, flops, world, dist, dev)
 
     # per-config figures (same method; parity-test configs, reported for the roofline)
     per_config = {}

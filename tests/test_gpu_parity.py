@@ -179,3 +179,18 @@ def test_split_tail_matches_unsplit(binding, dev, oracle_mod, kind):
         parity.assert_exact(ids_s, sc_s, r_ids, r_sc)
     else:
         parity.assert_close(ids_s, sc_s, small, np.arange(4))
+
+
+def test_eager_matches_prepared_on_a_split_tail(binding, dev):
+    """The eager entry runs the same three launches (scan, merge, selection) for a split tail."""
+    import torch
+
+    wl = inputs.draw(8, 7000, [0, 8], [0, 7000], 300, seed=13, kind="normal")
+    assert len(binding.indexer_topk_unit_table(binding.Desc(8, 7000, [0, 8], [0, 7000], 300))) > 2
+    ids0, sc0 = run_plan(binding, wl, dev)
+    q, k, w = parity.to_device(wl, dev)
+    ids1, sc1 = binding.indexer_topk(q, k, w, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.top_k)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(ids1.cpu().numpy(), ids0)
+    np.testing.assert_array_equal(sc1.cpu().numpy().view(np.uint32), sc0.view(np.uint32))
+    parity.assert_close(ids0, sc0, wl, np.arange(8))

@@ -56,7 +56,9 @@ def test_noalloc_matches_prepared_on_two_calls(env):
     second = inputs.draw(900, 900, [0, 900], [0, 900], 256, seed=32, kind="int")
     # more than 512 work units: the static candidate store takes them in two launch pairs
     third = inputs.draw(2600, 3000, [0, 1300, 2600], [0, 1500, 3000], 128, seed=33, kind="normal")
-    for wl in (first, second, third):
+    # a split tail: 8 queries over 6000 keys (two blocks of 12 units, then a merge launch)
+    fourth = inputs.draw(8, 6000, [0, 8], [0, 6000], 512, seed=34, kind="int")
+    for wl in (first, second, third, fourth):
         q, k, w = parity.to_device(wl, dev)
         ref_ids, ref_sc = _prepared(binding, torch, dev, wl, q, k, w)
         got_ids, got_sc = _noalloc(binding, torch, dev, wl, q, k, w)
