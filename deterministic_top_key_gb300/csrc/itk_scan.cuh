@@ -36,9 +36,9 @@
 // (top 11 bits of the order-preserving score key) at or above a threshold bin; the
 // threshold bin is the highest bin whose bins-at-or-above hold at least top_k appended
 // keys. It only rises, and every key it rejects is below top_k keys already seen, so the
-// buffer always contains the exact top-k of the keys seen so far. Every count of that
-// histogram is at most the buffer capacity (keys of bins below the threshold are never
-// appended again), so 16-bit counters, two to a word, suffice.
+// buffer always contains the exact top-k of the keys seen so far. The filter compares
+// the score itself with the lowest score of the threshold bin, and forms the 64-bit key
+// only for the keys it appends.
 #pragma once
 
 #include "itk_common.cuh"
@@ -65,8 +65,8 @@ constexpr uint32_t kKStageBytes = 2 * kKHalfBytes;       // 32 KB
 // Shared memory layout (offsets from a 1024-byte aligned base).
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
-constexpr uint32_t kOffHist = kOffK + kStages * kKStageBytes;          // 4 queries x 1024 words (2 x u16 bins)
-constexpr uint32_t kOffW = kOffHist + kQB * (kBins / 2) * 4;           // 4 queries x 64 floats
+constexpr uint32_t kOffHist = kOffK + kStages * kKStageBytes;          // 4 queries x 2048 u32 bins
+constexpr uint32_t kOffW = kOffHist + kQB * kBins * 4;                 // 4 queries x 64 floats
 constexpr uint32_t kOffRadix = kOffW + kQB * kHeads * 4;               // 4 groups x 256 x u32
 constexpr uint32_t kOffQState = kOffRadix + kEpiGroups * 256 * 4;      // 4 queries x 4 x u32
 constexpr uint32_t kOffSel = kOffQState + kQB * 16;                    // 4 groups x 8 x u32
@@ -82,7 +82,6 @@ static_assert(kOffK % 1024 == 0 && kKStageBytes % 1024 == 0 && kQHalfBytes % 102
 static_assert(kOffBar % 8 == 0 && kOffW % 16 == 0 && kOffUnit % 16 == 0, "alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kMaxTopK <= static_cast<int>(kCompactAt), "a compaction to top_k must leave room for the next tiles");
-static_assert(kQCap < 65536, "16-bit histogram counters");
 
 struct ScanParams {
   const UnitDesc* units;
@@ -128,11 +127,9 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
-// Packed 16-bit histogram (two bins per 32-bit word).
-__device__ __forceinline__ uint32_t hist16_get(const uint32_t* h, uint32_t b) {
-  return (h[b >> 1] >> ((b & 1u) * 16u)) & 0xFFFFu;
-}
-__device__ __forceinline__ void hist16_inc(uint32_t* h, uint32_t b) { atomicAdd(&h[b >> 1], 1u << ((b & 1u) * 16u)); }
+// Per-query histogram of appended score keys: one 32-bit counter per bin.
+__device__ __forceinline__ uint32_t hist_get(const uint32_t* h, uint32_t b) { return h[b]; }
+__device__ __forceinline__ void hist_inc(uint32_t* h, uint32_t b) { atomicAdd(&h[b], 1u); }
 
 // Radix select streamed from global memory, one byte per pass: returns `prefix` with
 // #{x in buf[0..n) : x >= prefix} == K (K <= n, keys distinct). Used only when ties crowd
@@ -187,12 +184,12 @@ __device__ __forceinline__ uint32_t group_keep_at_or_above(const GroupCtx& c, co
 __device__ uint32_t group_exact_in_place(const GroupCtx& c, unsigned long long* buf, uint32_t n, uint32_t* hist,
                                          uint32_t K, uint32_t* s_cursor, unsigned long long* scratch) {
   const unsigned long long prefix = group_select_stream(c, buf, n, K);
-  for (int i = c.gtid; i < kBins / 2; i += 128) hist[i] = 0u;
+  for (int i = c.gtid; i < kBins; i += 128) hist[i] = 0u;
   group_keep_at_or_above(c, buf, n, prefix, scratch, K, s_cursor);
   for (uint32_t i = c.gtid; i < K; i += 128) {
     const unsigned long long x = scratch[i];
     buf[i] = x;
-    hist16_inc(hist, bin_of(x));
+    hist_inc(hist, bin_of(x));
   }
   gsync(c);
   return bin_of(prefix);
@@ -282,15 +279,15 @@ __device__ __forceinline__ void warp_raise_threshold(uint32_t* qs, const uint32_
   uint32_t ge = qs[3] + (n - qs[1]);
   uint32_t thr = qs[2];
   if (ge >= K) {
-    // fast skip over empty runs of 64 bins (one packed word per lane, conflict-free)
-    while ((thr & 1u) == 0 && thr + 64 < static_cast<uint32_t>(kBins)) {
-      const uint32_t word = hist[(thr >> 1) + static_cast<uint32_t>(lane)];
+    // fast skip over empty runs of 32 bins (one counter per lane, conflict-free)
+    while (thr + 32 < static_cast<uint32_t>(kBins)) {
+      const uint32_t word = hist[thr + static_cast<uint32_t>(lane)];
       if (__any_sync(0xFFFFFFFFu, word != 0u)) break;
-      thr += 64;
+      thr += 32;
     }
     while (true) {
       const uint32_t b = thr + static_cast<uint32_t>(lane);
-      const uint32_t h = b < static_cast<uint32_t>(kBins) ? hist16_get(hist, b) : 0u;
+      const uint32_t h = b < static_cast<uint32_t>(kBins) ? hist_get(hist, b) : 0u;
       uint32_t incl = h;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -510,7 +507,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     const uint32_t K = static_cast<uint32_t>(p.top_k);
     const uint64_t pol_cand = policy_evict_last();   // working buffers: reused unit after unit
     const uint64_t pol_store = policy_evict_first();  // candidate store: read only by the next kernel
-    uint32_t* hist_g = reinterpret_cast<uint32_t*>(smem + kOffHist) + g * (kBins / 2);
+    uint32_t* hist_g = reinterpret_cast<uint32_t*>(smem + kOffHist) + g * kBins;
     uint32_t* qs = s_qs + g * 4;
     const float4* wv = reinterpret_cast<const float4*>(s_w + g * kHeads);
     unsigned long long* cand = p.cand + static_cast<size_t>(blockIdx.x) * kCandKeysPerCta + static_cast<size_t>(g) * kQCap;
@@ -537,13 +534,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int4 range = s_unit[2 * slot + 1];
       const size_t uidx = static_cast<size_t>(range.x);
       if (c.gtid < kHeads) s_w[g * kHeads + c.gtid] = active ? p.w[static_cast<size_t>(unit.x + g) * kHeads + c.gtid] : 0.f;
-      for (int i = c.gtid; i < kBins / 2; i += 128) hist_g[i] = 0u;
+      for (int i = c.gtid; i < kBins; i += 128) hist_g[i] = 0u;
       if (c.gtid < 4) qs[c.gtid] = 0u;
       gsync(c);
       const int tile0 = range.y, nt = range.z - range.y;
       const int last_key = unit.w + g;  // causal bound: local keys 0..last_key are visible
       bool failed = false;
       uint32_t thr = 0u;  // threshold bin, refreshed at every sync point
+      float thr_f = -__int_as_float(0x7F800000);  // the lowest score of bin thr (bins below 4 hold no finite score)
       for (int tile = 0; tile < nt; ++tile, ++ac) {
         const int ab = ac & 1;
         if (tile % kSyncEvery == sync_phase) {
@@ -561,6 +559,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (qs[0] > kCompactAt)
               epi_compact(c, cand, qs, hist_g, K, &s_pos[g], pol_cand, kCompactAt, exact_scratch);
             thr = qs[2];
+            thr_f = thr < 4u ? -__int_as_float(0x7F800000) : key_to_float(thr << kBinShift);
           }
         }
         if (!mbar_wait(bars.af(ab), (ac >> 1) & 1, s_abort)) {
@@ -570,7 +569,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         tc_fence_after_sync();
         const int jl = (tile0 + tile) * kBlockKeys + key_lane;  // local key index within the segment
-        uint32_t key32 = 0u;
+        float score = 0.f;
         if (active) {
           const uint32_t col = static_cast<uint32_t>(ab * kN + g * kHeads);
           float ps[8];
@@ -599,15 +598,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               ffma2(ps[6], ps[7], wb.z, wb.w, r6, r7);
             }
           }
-          const float score = (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]))) + 0.0f;
-          key32 = ord_key(score);
+          score = (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]))) + 0.0f;
         }
         // the accumulator buffer is read: hand it back to the MMA
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.ae(ab));
         // append the keys that pass the filter
-        const bool ins = active && jl <= last_key && (key32 >> kBinShift) >= thr;
+        const bool ins = active && jl <= last_key && score >= thr_f;  // == bin(score) >= thr for finite scores
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, ins);
         if (m) {
           const int lead = __ffs(m) - 1;
@@ -615,9 +613,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           if (lane == lead) base = atomicAdd(&qs[0], static_cast<uint32_t>(__popc(m)));
           base = __shfl_sync(0xFFFFFFFFu, base, lead);
           if (ins) {
+            const uint32_t key32 = ord_key(score);
             st_hint_u64(cand + base + __popc(m & ((1u << lane) - 1u)),
                         (static_cast<unsigned long long>(key32) << 32) | static_cast<uint32_t>(unit.z + jl), pol_cand);
-            hist16_inc(hist_g, key32 >> kBinShift);
+            hist_inc(hist_g, key32 >> kBinShift);
           }
         }
       }
