@@ -30,6 +30,7 @@ constexpr int kCap = 4096;                   // candidates per query handed from
 constexpr int kPerThread = kCap / 128;       // candidates a 128-thread group holds per thread
 constexpr int kBinShift = 21;                // histogram bin = top 11 bits of the 32-bit score key
 constexpr int kBins = 1 << (32 - kBinShift); // 2048 bins
+constexpr int kMaxMergeChunks = 256;         // chunks (units) a split query's keys may span
 
 constexpr uint32_t kStatusTimeout = 10u;   // matches ITK_ERR_DEVICE_TIMEOUT
 constexpr uint32_t kStatusInternal = 11u;  // matches ITK_ERR_INTERNAL

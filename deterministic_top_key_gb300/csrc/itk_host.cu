@@ -57,6 +57,7 @@ struct Layout {
 constexpr int kSplitMaxBlocks = 64;
 constexpr int kSplitTiles = 4;
 constexpr int kSplitUnits = 256;
+static_assert(kSplitUnits <= itk::kMaxMergeChunks, "a split query's chunks fit the merge's count table");
 
 int build_layout(const itk_desc* d, Layout* out) {
   if (!d) return fail(ITK_ERR_INVALID_ARGUMENT, "descriptor is NULL");
@@ -349,7 +350,7 @@ int launch_run(const Layout& L, int grid, int sm_count, const RunTables& t, cons
     mp.store = prm.store;
     mp.counts = prm.counts;
     mp.status = t.status;
-    itk::indexer_topk_merge_kernel<<<static_cast<int>(t.n_merges), itk::kMergeThreads, 0, stream>>>(mp);
+    itk::indexer_topk_merge_kernel<<<static_cast<int>(t.n_merges) * itk::kMergeCluster, itk::kMergeThreads, 0, stream>>>(mp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   }

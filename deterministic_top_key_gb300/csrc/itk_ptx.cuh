@@ -1,5 +1,6 @@
-// Inline-PTX wrappers for sm_103a: mbarrier, TMA tensor loads and the 5th-generation
-// tensor core (tcgen05: TMEM allocation, MMA, commit, TMEM loads).
+// Inline-PTX wrappers for sm_103a: mbarrier, TMA tensor loads, the 5th-generation
+// tensor core (tcgen05: TMEM allocation, MMA, commit, TMEM loads) and cluster
+// barriers with distributed shared memory.
 //
 // Every wait here is bounded: it gives up after kWaitLimitCycles SM clocks (about one
 // second) or as soon as the CTA's abort flag is raised, and reports the give-up to the
@@ -179,6 +180,32 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- thread-block clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Full cluster barrier: every thread of every CTA in the cluster arrives (release) and
+// waits (acquire), so shared and global writes before it are visible to the cluster after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 
 }  // namespace itk

@@ -328,12 +328,24 @@ __global__ void __launch_bounds__(kSelThreads, 1) indexer_topk_select_kernel(con
 
 // ------------------------------------------------------------------ split-query merge
 // A query whose visible keys were scanned by several units (a split tail) has one
-// candidate list per unit. One 256-thread CTA per such query histograms the union over
-// the 2048 score bins, keeps every key in the bins that reach the first top_k positions
-// when that fits in kCap, and otherwise keeps exactly the top_k keys (a radix select on
-// the bits below the bin inside the crossing bin). The result goes to the query's own
-// store slot, which the selection kernel then sorts like any other.
-constexpr int kMergeThreads = 256;
+// candidate list per unit. A cluster of kMergeCluster CTAs per such query reduces the
+// union to at most kCap keys that contain its top_k: it looks for the threshold key t
+// with #{x >= t} in [top_k, kCap] by a radix search on the 64-bit selection key, 11 bits
+// (2048 digits) per level from the top. At each level every CTA counts the digits of its
+// share of the keys that match the prefix fixed so far, the cluster adds the counts
+// through distributed shared memory (every CTA sums all of them, so all take the same
+// decision), and the digit that reaches position top_k is fixed. The search stops at the
+// first level where the keys at or above the digit fit in kCap: the first level already,
+// unless the score bin that crosses position top_k is crowded. Every CTA then appends its
+// keys >= t to the query's own store slot, which the selection kernel sorts like any other.
+constexpr int kMergeCluster = 8;
+constexpr int kMergeThreads = 512;
+constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMergeBatch = 8;     // chunks from which a thread loads a key before using any
+constexpr int kDigitBits = 11;
+constexpr int kDigits = 1 << kDigitBits;
+static_assert(kDigits == 4 * kMergeThreads, "each thread sums four digits");
+static_assert(kDigits == kBins, "the first level's digit is the score bin");
 
 struct MergeParams {
   const MergeDesc* merges;
@@ -345,123 +357,154 @@ struct MergeParams {
   uint32_t* status;
 };
 
-__global__ void __launch_bounds__(kMergeThreads) indexer_topk_merge_kernel(const MergeParams p) {
-  __shared__ uint32_t hist[kBins];
-  __shared__ uint32_t radix[256];
-  __shared__ uint32_t sel[8];
-  __shared__ uint32_t wsum[kMergeThreads / 32];
-  __shared__ uint32_t s_cursor;
+// Adds one to h[d] for every lane with v; lanes with the same digit share one atomic.
+__device__ __forceinline__ void hist_add_aggregated(uint32_t* h, uint32_t d, bool v, int lane) {
+  const uint32_t act = __ballot_sync(0xFFFFFFFFu, v);
+  if (v) {
+    const uint32_t peers = __match_any_sync(act, d);
+    if (lane == __ffs(peers) - 1) atomicAdd(&h[d], static_cast<uint32_t>(__popc(peers)));
+  }
+}
+
+__global__ void __cluster_dims__(kMergeCluster, 1, 1) __launch_bounds__(kMergeThreads, 1)
+    indexer_topk_merge_kernel(const MergeParams p) {
+  __shared__ __align__(16) uint32_t hist[2][kDigits];  // per level, alternating
+  __shared__ uint32_t s_cnt[kMaxMergeChunks];
+  __shared__ uint32_t wsum[kMergeWarps];
+  __shared__ uint32_t sel[4];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const MergeDesc m = p.merges[blockIdx.x];
-  const uint32_t K = static_cast<uint32_t>(p.top_k);
-  GroupCtx c;  // warp 0 picks radix digits, as in a 128-thread group
-  c.gtid = tid;
-  c.gwarp = warp;
-  c.lane = lane;
-  c.bar = 0;
-  c.radix = radix;
-  c.sel = sel;
+  const uint32_t rank = cluster_ctarank();
+  const MergeDesc m = p.merges[blockIdx.x / kMergeCluster];
+  int n_chunks = m.n_chunks;
+  if (n_chunks > kMaxMergeChunks) {  // the host never builds one; keep the walk in bounds
+    if (rank == 0 && tid == 0) atomicOr(p.status, kStatusInternal | (21u << 8));
+    n_chunks = kMaxMergeChunks;
+  }
   auto chunk_slot = [&](int ch) { return static_cast<size_t>(m.first_unit + ch) * kQB + m.j; };
-  auto chunk_count = [&](int ch) {
+  for (int ch = tid; ch < n_chunks; ch += kMergeThreads) {
     const uint32_t n = p.counts[chunk_slot(ch)];
-    return n < static_cast<uint32_t>(kCap) ? n : static_cast<uint32_t>(kCap);
-  };
-  for (int i = tid; i < kBins; i += kMergeThreads) hist[i] = 0u;
-  __syncthreads();
-  for (int ch = 0; ch < m.n_chunks; ++ch) {
-    const unsigned long long* src = p.store + chunk_slot(ch) * kCap;
-    const uint32_t n = chunk_count(ch);
-    for (uint32_t i = tid; i < n; i += kMergeThreads) atomicAdd(&hist[bin_of(src[i])], 1u);
+    s_cnt[ch] = n < static_cast<uint32_t>(kCap) ? n : static_cast<uint32_t>(kCap);
   }
+  uint32_t* cursor = p.counts + m.out_slot;  // append cursor, ends as the merged count
+  if (rank == 0 && tid == 0) *cursor = 0u;   // ordered before any append by the cluster barriers
   __syncthreads();
-  // ge(b) = keys in bins >= b: each thread sums 8 bins, highest bins first
-  constexpr int kPer = kBins / kMergeThreads;
-  uint32_t loc[kPer];
-  uint32_t s = 0;
+
+  // Visits this CTA's share of the union (chunk ch belongs to CTA ch % kMergeCluster),
+  // loading one key from each of up to kMergeBatch chunks before using any of them.
+  // f(x, v) is called by every thread of the CTA the same number of times.
+  auto for_union = [&](auto&& f) {
+    for (int c0 = static_cast<int>(rank); c0 < n_chunks; c0 += kMergeBatch * kMergeCluster) {
+      uint32_t cmax = 0;
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    loc[i] = hist[kBins - 1 - (kPer * tid + i)];
-    s += loc[i];
-  }
-  uint32_t incl = s;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-    if (lane >= off) incl += t;
-  }
-  if (lane == 31) wsum[warp] = incl;
-  if (tid == 0) sel[3] = 0u;  // tstar: the lowest bin kept (0 when fewer than K keys in all)
-  __syncthreads();
-  uint32_t run = incl - s;
-  for (int wv = 0; wv < warp; ++wv) run += wsum[wv];
-  __syncthreads();  // every thread has its run before hist is rewritten
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const uint32_t b = kBins - 1 - (kPer * tid + i);
-    const uint32_t above = run;  // keys in bins > b
-    run += loc[i];
-    hist[b] = run;               // now ge(b)
-    if (above < K && run >= K) sel[3] = b;  // the bin that reaches position K (at most one)
-  }
-  __syncthreads();
-  const uint32_t tstar = sel[3];
-  const uint32_t ge_t = hist[tstar];
-  const uint32_t ge_above = tstar + 1 < static_cast<uint32_t>(kBins) ? hist[tstar + 1] : 0u;
-  __syncthreads();
-  unsigned long long thr_key = static_cast<unsigned long long>(tstar) << (32 + kBinShift);
-  if (ge_t > static_cast<uint32_t>(kCap)) {
-    // exactly K: keys above bin tstar plus the (K - ge_above) largest inside bin tstar,
-    // found by a radix select on the 53 bits below the bin (shifted to the top)
-    unsigned long long prefix = 0ull;
-    uint32_t k_rem = K - ge_above;
-    for (int shift = 56; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += kMergeThreads) radix[i] = 0u;
-      __syncthreads();
-      const unsigned long long hi_mask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
-      for (int ch = 0; ch < m.n_chunks; ++ch) {
-        const unsigned long long* src = p.store + chunk_slot(ch) * kCap;
-        const uint32_t n = chunk_count(ch);
-        for (uint32_t i = tid; i < n; i += kMergeThreads) {
-          const unsigned long long x = src[i];
-          const unsigned long long y = x << (32 - kBinShift);  // the bits below the bin
-          if (bin_of(x) == tstar && (y & hi_mask) == (prefix & hi_mask)) atomicAdd(&radix[(y >> shift) & 0xFFu], 1u);
-        }
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const int ch = c0 + u * kMergeCluster;
+        if (ch < n_chunks) cmax = max(cmax, s_cnt[ch]);
       }
-      __syncthreads();
-      group_pick_digit(c, k_rem);
-      __syncthreads();
-      prefix |= static_cast<unsigned long long>(sel[0]) << shift;
-      k_rem = sel[1];
-      const uint32_t cnt = sel[2];
-      __syncthreads();
-      if (cnt == k_rem) break;  // uniform
+      for (uint32_t base = 0; base < cmax; base += kMergeThreads) {
+        const uint32_t off = base + static_cast<uint32_t>(tid);
+        unsigned long long x[kMergeBatch];
+        bool v[kMergeBatch];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+          const int ch = c0 + u * kMergeCluster;
+          v[u] = ch < n_chunks && off < s_cnt[ch];
+          x[u] = v[u] ? __ldcg(p.store + chunk_slot(ch) * kCap + off) : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) f(x[u], v[u]);
+      }
     }
-    thr_key |= prefix >> (32 - kBinShift);
+  };
+
+  const uint32_t K = static_cast<uint32_t>(p.top_k);
+  uint32_t k_rem = K;             // positions still to fill from the keys that match prefix
+  uint32_t above = 0;             // keys above the prefix's range (all kept)
+  unsigned long long prefix = 0;  // bits [hi, 64) fixed so far
+  unsigned long long thr = 0;
+  uint32_t kept = 0;
+  int hi = 64;
+  for (int level = 0;; ++level) {
+    const int shift = hi > kDigitBits ? hi - kDigitBits : 0;
+    uint32_t* h = hist[level & 1];
+    for (int i = tid; i < kDigits; i += kMergeThreads) h[i] = 0u;
+    __syncthreads();
+    for_union([&](unsigned long long x, bool v) {
+      const bool match = v && (hi >= 64 || (x >> hi) == (prefix >> hi));
+      hist_add_aggregated(h, static_cast<uint32_t>(x >> shift) & (kDigits - 1), match, lane);
+    });
+    cluster_sync_all();  // every CTA's counts for this level are complete
+    // Cluster-wide counts of the digits 2047-4t .. 2044-4t (thread t, descending).
+    uint32_t c4[4];
+    {
+      const uint32_t addr = smem_u32(h + (kDigits - 4 - 4 * tid));
+      uint4 acc = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int r = 0; r < kMergeCluster; ++r) {
+        const uint4 t = ld_dsmem_v4(mapa_shared(addr, static_cast<uint32_t>(r)));
+        acc.x += t.x;
+        acc.y += t.y;
+        acc.z += t.z;
+        acc.w += t.w;
+      }
+      c4[0] = acc.w;
+      c4[1] = acc.z;
+      c4[2] = acc.y;
+      c4[3] = acc.x;
+    }
+    const uint32_t s = c4[0] + c4[1] + c4[2] + c4[3];
+    uint32_t incl = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += t;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    uint32_t run = incl - s;  // matching keys in digits above this thread's four
+    uint32_t total = 0;
+    for (int wv = 0; wv < kMergeWarps; ++wv) {
+      if (wv < warp) run += wsum[wv];
+      total += wsum[wv];
+    }
+    if (tid == 0) {  // fewer matching keys than positions left (first level only): keep all
+      sel[0] = 0u;
+      sel[1] = total;
+      sel[2] = total;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t a = run;  // matching keys in digits above d
+      run += c4[i];
+      if (a < k_rem && run >= k_rem) {  // the digit that reaches position k_rem (at most one)
+        sel[0] = static_cast<uint32_t>(kDigits - 1 - (4 * tid + i));
+        sel[1] = run;
+        sel[2] = a;
+      }
+    }
+    __syncthreads();
+    const uint32_t dstar = sel[0], ge_d = sel[1], ge_above = sel[2];
+    if (above + ge_d <= static_cast<uint32_t>(kCap) || shift == 0) {
+      thr = prefix | (static_cast<unsigned long long>(dstar) << shift);
+      kept = above + ge_d;
+      break;
+    }
+    above += ge_above;
+    k_rem -= ge_above;
+    prefix |= static_cast<unsigned long long>(dstar) << shift;
+    hi = shift;
   }
+
   // keep every key at or above the threshold key
-  if (tid == 0) s_cursor = 0u;
-  __syncthreads();
   unsigned long long* dst = p.store + static_cast<size_t>(m.out_slot) * kCap;
-  for (int ch = 0; ch < m.n_chunks; ++ch) {
-    const unsigned long long* src = p.store + chunk_slot(ch) * kCap;
-    const uint32_t n = chunk_count(ch);
-    for (uint32_t base = 0; base < n; base += kMergeThreads) {
-      const uint32_t i = base + tid;
-      const unsigned long long x = i < n ? src[i] : 0ull;
-      const bool keep = i < n && x >= thr_key;
-      const uint32_t slot = warp_append_slot(keep, &s_cursor, lane);
-      if (keep && slot < static_cast<uint32_t>(kCap)) dst[slot] = x;
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    uint32_t n = s_cursor;
-    if (n > static_cast<uint32_t>(kCap)) {  // cannot happen: at most max(ge_t, K) <= kCap keys qualify
-      atomicOr(p.status, kStatusInternal | (22u << 8));
-      n = kCap;
-    }
-    p.counts[m.out_slot] = n;
-  }
+  for_union([&](unsigned long long x, bool v) {
+    const bool keep = v && x >= thr;
+    const uint32_t slot = warp_append_slot(keep, cursor, lane);
+    if (keep && slot < static_cast<uint32_t>(kCap)) dst[slot] = x;
+  });
+  if (rank == 0 && tid == 0 && kept > static_cast<uint32_t>(kCap))  // cannot happen: keys are distinct
+    atomicOr(p.status, kStatusInternal | (22u << 8));
+  cluster_sync_all();  // no CTA leaves while another may still read its counts
 }
 
 }  // namespace itk

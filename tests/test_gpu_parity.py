@@ -123,6 +123,18 @@ def test_monotone_and_tied_scores(binding, dev, oracle_mod, direction):
     parity.assert_exact(ids, sc, r_ids, r_sc)
 
 
+@pytest.mark.parametrize("direction", [1, -1, 0])
+def test_monotone_and_tied_scores_on_a_split_tail(binding, dev, oracle_mod, direction):
+    """Four queries over 9000 keys run as a split tail (18 units). With all-equal scores
+    every key lands in one score bin, so the merge narrows its threshold over several
+    digit levels, down to the key ids; monotone scores keep every key of a chunk."""
+    wl = _monotone_problem(9000, 4, direction, 2048)
+    assert len(binding.indexer_topk_unit_table(binding.Desc(4, 9000, [0, 4], [0, 9000], 2048))) > 2
+    ids, sc = run_plan(binding, wl, dev)
+    r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl))
+    parity.assert_exact(ids, sc, r_ids, r_sc)
+
+
 def test_repeat_runs_bit_identical(binding, dev):
     wl = inputs.draw(200, 1500, [0, 200], [0, 1500], 256, seed=4, kind="normal")
     outs = run_plan(binding, wl, dev, runs=3)
