@@ -63,6 +63,15 @@ def row_visible(wl) -> np.ndarray:
     return out
 
 
+def finish_kernels(binding, wl) -> str:
+    """The launches after the scan: the merge for split queries, the selection for the rest."""
+    ut = binding.indexer_topk_unit_table(binding.Desc(wl.T, wl.Tkv, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.top_k,
+                                                      wl.q_causal_offsets))
+    _, per_block = np.unique(ut[:, 0], return_counts=True)
+    names = (["merge"] if (per_block > 1).any() else []) + (["selection"] if (per_block == 1).any() else [])
+    return " + ".join(names)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -309,9 +318,6 @@ def _measure(binding, torch, wl, dev, steps, warmup, flush_buf):
     return plan, (q, k, w, ids, sc, ws), stream
 
 
-KERNELS_PER_STEP = 2  # the scan kernel, then the selection kernel
-
-
 def _timed_steps(binding, torch, plan, bufs, stream, steps, flush_buf):
     """Times `steps` runs with CUDA events on the launching stream: per step the whole call
     (start..end) and, through the library's split event recorded between its two launches,
@@ -542,8 +548,8 @@ def run_ours(args):
         tf2 = f2 / (m2 * 1e-3) / 1e12
         tf2_scan = f2 / (m2_scan * 1e-3) / 1e12
         per_config[name] = {"ms": m2, "tflops": tf2, "frac": tf2 / peaks["bf16_tflops"],
-                            "scan_ms": m2_scan, "scan_frac": tf2_scan / peaks["bf16_tflops"], "select_ms": m2_sel,
-                            "T": wl2.T, "Tkv": wl2.Tkv}
+                            "scan_ms": m2_scan, "scan_frac": tf2_scan / peaks["bf16_tflops"], "finish_ms": m2_sel,
+                            "finish": finish_kernels(binding, wl2), "T": wl2.T, "Tkv": wl2.Tkv}
         plan2.destroy()
         del b2
 
@@ -553,6 +559,7 @@ def run_ours(args):
             dist.destroy_process_group()
         return 0
 
+    finish = [{"merge": "merge", "selection": "select"}[f] for f in finish_kernels(binding, wl).split(" + ")]
     achieved = flops / (scan_ms * 1e-3) / 1e12  # the dominant kernel alone
     traffic = load_traffic()
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -572,9 +579,9 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(wl, world),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(),
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": (1 + len(finish)) * args.steps,
         "kernels": {"indexer_topk_scan_kernel": {"ms": scan_ms, "launches": args.steps},
-                    "indexer_topk_select_kernel": {"ms": sel_ms, "launches": args.steps}},
+                    " + ".join(f"indexer_topk_{f}_kernel" for f in finish): {"ms": sel_ms, "launches": args.steps}},
         "per_config": per_config, "wall_s_timed_region": wall,
     }
     print(json.dumps(line), flush=True)

@@ -45,13 +45,13 @@ struct UnitDesc {
 };
 
 // A query whose visible keys were split over several units: its candidates sit in the
-// store slots (unit u, query j) for u in [first_unit, first_unit + n_chunks) and are
-// merged into the slot `out_slot` before the selection.
+// store slots (unit u, query j) for u in [first_unit, first_unit + n_chunks); the merge
+// selects its top_k from their union and writes output row `row`.
 struct MergeDesc {
   int32_t first_unit;
   int32_t n_chunks;
-  int32_t j;         // query index within the units (0..3)
-  int32_t out_slot;  // store slot of the merged candidates
+  int32_t j;    // query index within the units (0..3)
+  int32_t row;  // output row of the query
 };
 
 // Self-resetting work counter: CTAs draw items with atomicAdd on `next`; the last CTA to

@@ -47,7 +47,8 @@ struct Layout {
   std::vector<UnitDesc> units;     // ticket order: most key tiles first
   std::vector<int32_t> item_rows;  // per store slot: output row, or -1 (empty or merged elsewhere)
   std::vector<itk::MergeDesc> merges;
-  size_t n_slots() const { return item_rows.size(); }  // units * 4 + merges
+  size_t select_rows = 0;          // item rows >= 0: queries the selection kernel finishes
+  size_t n_slots() const { return item_rows.size(); }  // units * 4
 };
 
 // Split tails: a descriptor with at most kSplitMaxBlocks query blocks cannot fill the
@@ -128,8 +129,11 @@ int build_layout(const itk_desc* d, Layout* out) {
         u.tile0 = static_cast<int32_t>(it.tiles * c / chunks);
         u.tile1 = static_cast<int32_t>(it.tiles * (c + 1) / chunks);
         L.units.push_back(u);
-        for (int j = 0; j < itk::kQB; ++j)
-          L.item_rows.push_back(chunks == 1 && j < u.nq ? u.q_row0 + j : -1);
+        for (int j = 0; j < itk::kQB; ++j) {
+          const bool own = chunks == 1 && j < u.nq;  // split queries are finished by the merge
+          L.item_rows.push_back(own ? u.q_row0 + j : -1);
+          L.select_rows += own ? 1 : 0;
+        }
       }
       if (chunks > 1)
         for (int j = 0; j < it.u.nq; ++j) {
@@ -137,15 +141,9 @@ int build_layout(const itk_desc* d, Layout* out) {
           m.first_unit = first;
           m.n_chunks = static_cast<int32_t>(chunks);
           m.j = j;
-          m.out_slot = -1;  // set below, once the number of unit slots is known
+          m.row = it.u.q_row0 + j;
           L.merges.push_back(m);
         }
-    }
-    const int32_t unit_slots = static_cast<int32_t>(L.units.size()) * itk::kQB;
-    for (size_t m = 0; m < L.merges.size(); ++m) {
-      L.merges[m].out_slot = unit_slots + static_cast<int32_t>(m);
-      const UnitDesc& u = L.units[L.merges[m].first_unit];
-      L.item_rows.push_back(u.q_row0 + L.merges[m].j);
     }
   }
   *out = std::move(L);
@@ -240,8 +238,7 @@ std::vector<unsigned char> block_image(const Layout& L, const BlockLayout& b) {
 }
 
 // Workspace layout of one run: per-CTA working buffers of the scan, then the candidate
-// store (kCap keys per slot: four slots per unit, then one per merged query), then the
-// per-slot counts.
+// store (kCap keys per slot, four slots per unit), then the per-slot counts.
 struct WorkLayout {
   size_t cand_off = 0, store_off = 0, counts_off = 0, bytes = 0;
 };
@@ -262,6 +259,7 @@ struct RunTables {
   size_t n_slots = 0;
   const itk::MergeDesc* merges = nullptr;
   size_t n_merges = 0;
+  bool select = true;              // some slot has an output row (else no selection launch)
   TicketBlock* tickets = nullptr;  // two adjacent blocks: scan, selection
   uint32_t* status = nullptr;
 };
@@ -273,6 +271,7 @@ RunTables block_tables(const Layout& L, const BlockLayout& b, char* blk) {
   t.n_slots = L.item_rows.size();
   t.merges = reinterpret_cast<const itk::MergeDesc*>(blk + b.merges_off);
   t.n_merges = L.merges.size();
+  t.select = L.select_rows > 0;
   t.tickets = reinterpret_cast<TicketBlock*>(blk + b.ticket_off);
   t.status = reinterpret_cast<uint32_t*>(blk + b.status_off);
   return t;
@@ -289,6 +288,9 @@ int ensure_kernel_attributes() {
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(itk::indexer_topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSelSmemLaunch));
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(itk::indexer_topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(itk::kMergeSmemBytes));
   });
   if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute");
   return ITK_OK;
@@ -305,9 +307,9 @@ int check_run_buffers(const Layout& L, const void* q, const void* k, const float
   return ITK_OK;
 }
 
-// Encode maps and launch the scan over the units of `t`, the merge of split queries (if
-// any), then the selection of every slot with an output row. `work` is laid out by
-// work_layout(grid, t.n_slots).
+// Encode maps and launch the scan over the units of `t`, then the merge of split queries
+// (if any) and the selection of every slot with an output row (if any). `work` is laid
+// out by work_layout(grid, t.n_slots).
 int launch_run(const Layout& L, int grid, int sm_count, const RunTables& t, const void* q, const void* k,
                const float* w, int32_t* ids, float* scores, void* work, cudaStream_t stream,
                bool force_launch_failure, cudaEvent_t split_event = nullptr, bool static_schedule = false) {
@@ -346,14 +348,17 @@ int launch_run(const Layout& L, int grid, int sm_count, const RunTables& t, cons
     mp.merges = t.merges;
     mp.n_merges = static_cast<int32_t>(t.n_merges);
     mp.top_k = L.top_k;
-    mp.units = t.units;
     mp.store = prm.store;
     mp.counts = prm.counts;
     mp.status = t.status;
-    itk::indexer_topk_merge_kernel<<<static_cast<int>(t.n_merges) * itk::kMergeCluster, itk::kMergeThreads, 0, stream>>>(mp);
+    mp.out_ids = ids;
+    mp.out_scores = scores;
+    itk::indexer_topk_merge_kernel<<<static_cast<int>(t.n_merges) * itk::kMergeCluster, itk::kMergeThreads,
+                                     itk::kMergeSmemBytes, stream>>>(mp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   }
+  if (!t.select) return ITK_OK;
   itk::SelectParams sp;
   sp.item_rows = t.item_rows;
   sp.n_items = static_cast<int32_t>(t.n_slots);
@@ -660,12 +665,12 @@ constexpr int64_t kNoAllocMaxUnits = 65536;   // work units (4 queries each) the
 // query blocks, whose at most kSplitUnits + kSplitMaxBlocks units fit one launch pair.
 constexpr size_t kNoAllocMaxMerges = static_cast<size_t>(kSplitMaxBlocks) * itk::kQB;
 static_assert(kSplitUnits + kSplitMaxBlocks <= static_cast<int>(kNoAllocChunkUnits), "split runs fit one chunk");
-constexpr size_t kNoAllocChunkSlots = kNoAllocChunkUnits * itk::kQB + kNoAllocMaxMerges;
+constexpr size_t kNoAllocChunkSlots = kNoAllocChunkUnits * itk::kQB;
 constexpr size_t kNoAllocWorkBytes = work_layout(kNoAllocMaxCtas, kNoAllocChunkSlots).bytes;
 constexpr size_t kNoAllocUnitsOff = kNoAllocWorkBytes;
 constexpr size_t kNoAllocItemsOff = kNoAllocUnitsOff + align_up(kNoAllocMaxUnits * sizeof(UnitDesc), 256);
 constexpr size_t kNoAllocMergesOff =
-    kNoAllocItemsOff + align_up((kNoAllocMaxUnits * itk::kQB + kNoAllocMaxMerges) * sizeof(int32_t), 256);
+    kNoAllocItemsOff + align_up(kNoAllocMaxUnits * itk::kQB * sizeof(int32_t), 256);
 constexpr size_t kNoAllocTicketOff = kNoAllocMergesOff + align_up(kNoAllocMaxMerges * sizeof(itk::MergeDesc), 256);
 constexpr size_t kNoAllocStatusOff = kNoAllocTicketOff + 256;
 constexpr size_t kNoAllocBytes = kNoAllocStatusOff + 256;
@@ -737,9 +742,10 @@ int indexer_topk_run_noalloc(const itk_desc* desc, const void* q, const void* k,
     t.units = reinterpret_cast<const UnitDesc*>(scratch + kNoAllocUnitsOff) + u0;
     t.n_units = n;
     t.item_rows = reinterpret_cast<const int32_t*>(scratch + kNoAllocItemsOff) + u0 * itk::kQB;
-    t.n_slots = n * itk::kQB + (whole ? L.merges.size() : 0);
+    t.n_slots = n * itk::kQB;
     t.merges = reinterpret_cast<const itk::MergeDesc*>(scratch + kNoAllocMergesOff);
     t.n_merges = whole ? L.merges.size() : 0;
+    t.select = !whole || L.select_rows > 0;
     t.tickets = reinterpret_cast<TicketBlock*>(scratch + kNoAllocTicketOff);
     t.status = reinterpret_cast<uint32_t*>(scratch + kNoAllocStatusOff);
     // work_layout(grid, t.n_slots) of a chunk fits inside work_layout(kNoAllocMaxCtas, kNoAllocChunkSlots)

@@ -328,16 +328,22 @@ __global__ void __launch_bounds__(kSelThreads, 1) indexer_topk_select_kernel(con
 
 // ------------------------------------------------------------------ split-query merge
 // A query whose visible keys were scanned by several units (a split tail) has one
-// candidate list per unit. A cluster of kMergeCluster CTAs per such query reduces the
-// union to at most kCap keys that contain its top_k: it looks for the threshold key t
-// with #{x >= t} in [top_k, kCap] by a radix search on the 64-bit selection key, 11 bits
-// (2048 digits) per level from the top. At each level every CTA counts the digits of its
-// share of the keys that match the prefix fixed so far, the cluster adds the counts
-// through distributed shared memory (every CTA sums all of them, so all take the same
-// decision), and the digit that reaches position top_k is fixed. The search stops at the
-// first level where the keys at or above the digit fit in kCap: the first level already,
-// unless the score bin that crosses position top_k is crowded. Every CTA then appends its
-// keys >= t to the query's own store slot, which the selection kernel sorts like any other.
+// candidate list per unit. A cluster of kMergeCluster CTAs per such query selects its
+// top_k from the union and writes the output row; the selection kernel never sees it.
+// 1. Threshold: the cluster looks for the key t with #{x >= t} in [top_k, kCap] by a
+//    radix search on the 64-bit selection key, 11 bits (2048 digits) per level from the
+//    top. At each level every CTA counts the digits of its share of the keys that match
+//    the prefix fixed so far, the cluster adds the counts through distributed shared
+//    memory (every CTA sums all of them, so all take the same decision), and the digit
+//    that reaches position top_k is fixed. The search stops at the first level where the
+//    keys at or above the digit fit in kCap: the first level already, unless the score
+//    bin that crosses position top_k is crowded.
+// 2. Every CTA keeps its own keys >= t in shared memory and sorts them (bitonic,
+//    descending: shuffles inside a warp, shared memory across warps).
+// 3. Every CTA copies the cluster's sorted blocks into its shared memory. A key's
+//    position in the row is its index in its own block plus, for every other block, the
+//    number of keys above it there (a binary search). Keys are distinct, so the positions
+//    are those of the sorted union, whichever CTA holds which key.
 constexpr int kMergeCluster = 8;
 constexpr int kMergeThreads = 512;
 constexpr int kMergeWarps = kMergeThreads / 32;
@@ -347,14 +353,18 @@ constexpr int kDigits = 1 << kDigitBits;
 static_assert(kDigits == 4 * kMergeThreads, "each thread sums four digits");
 static_assert(kDigits == kBins, "the first level's digit is the score bin");
 
+// own sorted keys, then a copy of every CTA's (kCap keys each: all kept keys may sit in one CTA)
+constexpr uint32_t kMergeSmemBytes = 2 * kCap * sizeof(unsigned long long);
+
 struct MergeParams {
   const MergeDesc* merges;
   int32_t n_merges;
   int32_t top_k;
-  const UnitDesc* units;
-  unsigned long long* store;
-  uint32_t* counts;
+  const unsigned long long* store;
+  const uint32_t* counts;
   uint32_t* status;
+  int32_t* out_ids;     // [T, top_k]
+  float* out_scores;    // [T, top_k]
 };
 
 // Adds one to h[d] for every lane with v; lanes with the same digit share one atomic.
@@ -366,12 +376,76 @@ __device__ __forceinline__ void hist_add_aggregated(uint32_t* h, uint32_t d, boo
   }
 }
 
+// Sorts the first n (<= 512 * E) keys of buf in descending order, in place, with the
+// whole CTA: element e = 512 r + t sits in register v[r] of thread t; partners at index
+// distance j < 32 are exchanged by shuffles, 32 <= j < 512 through buf, j >= 512 inside
+// the thread. Entries n .. 512 E - 1 of buf are overwritten with zero keys (below every
+// key) and sort last.
+template <int E>
+__device__ void cta_sort_desc(unsigned long long* buf, uint32_t n) {
+  constexpr uint32_t kN = kMergeThreads * E;
+  const uint32_t t = threadIdx.x;
+  unsigned long long v[E];
+#pragma unroll
+  for (int r = 0; r < E; ++r) {
+    const uint32_t e = kMergeThreads * r + t;
+    v[r] = e < n ? buf[e] : 0ull;
+  }
+  for (uint32_t k = 2; k <= kN; k <<= 1) {
+    for (uint32_t j = k >> 1; j > 0; j >>= 1) {
+      if (j >= static_cast<uint32_t>(kMergeThreads)) {  // partner in the same thread
+#pragma unroll
+        for (int rj = 1; rj < E; rj <<= 1) {  // register indices stay compile-time constants
+          if (static_cast<uint32_t>(rj) * kMergeThreads != j) continue;
+#pragma unroll
+          for (int r = 0; r < E; ++r) {
+            if (r & rj) continue;
+            const uint32_t e = kMergeThreads * r + t;
+            const bool desc = (e & k) == 0;
+            const unsigned long long a = v[r], b = v[r | rj];
+            if ((a < b) == desc) {
+              v[r] = b;
+              v[r | rj] = a;
+            }
+          }
+        }
+      } else {
+        unsigned long long pv[E];
+        if (j < 32) {
+#pragma unroll
+          for (int r = 0; r < E; ++r) pv[r] = __shfl_xor_sync(0xFFFFFFFFu, v[r], static_cast<int>(j));
+        } else {
+#pragma unroll
+          for (int r = 0; r < E; ++r) buf[kMergeThreads * r + t] = v[r];
+          __syncthreads();
+#pragma unroll
+          for (int r = 0; r < E; ++r) pv[r] = buf[kMergeThreads * r + (t ^ j)];
+          __syncthreads();
+        }
+#pragma unroll
+        for (int r = 0; r < E; ++r) {
+          const uint32_t e = kMergeThreads * r + t;
+          const bool keep_max = ((e & j) == 0) == ((e & k) == 0);  // lower index of a descending pair, or upper of an ascending one
+          const unsigned long long a = v[r], b = pv[r];
+          v[r] = keep_max ? (a > b ? a : b) : (a < b ? a : b);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < E; ++r) buf[kMergeThreads * r + t] = v[r];
+  __syncthreads();
+}
+
 __global__ void __cluster_dims__(kMergeCluster, 1, 1) __launch_bounds__(kMergeThreads, 1)
     indexer_topk_merge_kernel(const MergeParams p) {
-  __shared__ __align__(16) uint32_t hist[2][kDigits];  // per level, alternating
+  extern __shared__ __align__(16) unsigned long long s_own[];  // kCap own keys, then kCap of the cluster's
+  unsigned long long* s_all = s_own + kCap;
+  __shared__ __align__(16) uint32_t hist[2][kDigits];            // per level, alternating
   __shared__ uint32_t s_cnt[kMaxMergeChunks];
   __shared__ uint32_t wsum[kMergeWarps];
   __shared__ uint32_t sel[4];
+  __shared__ uint32_t s_cursor;  // own keys kept in s_own
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
   const MergeDesc m = p.merges[blockIdx.x / kMergeCluster];
@@ -385,8 +459,7 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __launch_bounds__(kMergeTh
     const uint32_t n = p.counts[chunk_slot(ch)];
     s_cnt[ch] = n < static_cast<uint32_t>(kCap) ? n : static_cast<uint32_t>(kCap);
   }
-  uint32_t* cursor = p.counts + m.out_slot;  // append cursor, ends as the merged count
-  if (rank == 0 && tid == 0) *cursor = 0u;   // ordered before any append by the cluster barriers
+  if (tid == 0) s_cursor = 0u;
   __syncthreads();
 
   // Visits this CTA's share of the union (chunk ch belongs to CTA ch % kMergeCluster),
@@ -495,16 +568,71 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __launch_bounds__(kMergeTh
     hi = shift;
   }
 
-  // keep every key at or above the threshold key
-  unsigned long long* dst = p.store + static_cast<size_t>(m.out_slot) * kCap;
+  if (kept > static_cast<uint32_t>(kCap)) {  // cannot happen: keys are distinct
+    if (rank == 0 && tid == 0) atomicOr(p.status, kStatusInternal | (22u << 8));
+    kept = kCap;
+  }
+  // keep this CTA's keys at or above the threshold key
   for_union([&](unsigned long long x, bool v) {
     const bool keep = v && x >= thr;
-    const uint32_t slot = warp_append_slot(keep, cursor, lane);
-    if (keep && slot < static_cast<uint32_t>(kCap)) dst[slot] = x;
+    const uint32_t slot = warp_append_slot(keep, &s_cursor, lane);
+    if (keep && slot < static_cast<uint32_t>(kCap)) s_own[slot] = x;
   });
-  if (rank == 0 && tid == 0 && kept > static_cast<uint32_t>(kCap))  // cannot happen: keys are distinct
-    atomicOr(p.status, kStatusInternal | (22u << 8));
-  cluster_sync_all();  // no CTA leaves while another may still read its counts
+  __syncthreads();
+  const uint32_t n_own = min(s_cursor, static_cast<uint32_t>(kCap));
+  if (n_own <= kMergeThreads) cta_sort_desc<1>(s_own, n_own);
+  else if (n_own <= 2 * kMergeThreads) cta_sort_desc<2>(s_own, n_own);
+  else if (n_own <= 4 * kMergeThreads) cta_sort_desc<4>(s_own, n_own);
+  else cta_sort_desc<8>(s_own, n_own);
+  cluster_sync_all();  // every CTA's block is sorted and its count final
+
+  // copy the cluster's blocks (block r at offset off[r]) into s_all
+  uint32_t off[kMergeCluster + 1];
+  off[0] = 0;
+  const uint32_t cur_addr = smem_u32(&s_cursor);
+#pragma unroll
+  for (int r = 0; r < kMergeCluster; ++r) {
+    const uint32_t c = ld_dsmem_u32(mapa_shared(cur_addr, static_cast<uint32_t>(r)));
+    off[r + 1] = min(off[r] + min(c, static_cast<uint32_t>(kCap)), static_cast<uint32_t>(kCap));
+  }
+  const uint32_t own_addr = smem_u32(s_own);
+#pragma unroll
+  for (int r = 0; r < kMergeCluster; ++r) {
+    const uint32_t base = mapa_shared(own_addr, static_cast<uint32_t>(r));
+    for (uint32_t i = off[r] + tid; i < off[r + 1]; i += kMergeThreads)
+      s_all[i] = ld_dsmem_u64(base + (i - off[r]) * 8u);
+  }
+  cluster_sync_all();  // no CTA reads another's shared memory after this
+  // positions of this CTA's keys in the merged row
+  const uint32_t keff = kept < K ? kept : K;
+  int32_t* out_ids = p.out_ids + static_cast<size_t>(m.row) * K;
+  float* out_scores = p.out_scores + static_cast<size_t>(m.row) * K;
+  for (uint32_t e = tid; e < n_own; e += kMergeThreads) {
+    const unsigned long long x = s_own[e];
+    uint32_t pos = e;
+#pragma unroll
+    for (int r = 0; r < kMergeCluster; ++r) {
+      if (r == static_cast<int>(rank)) continue;
+      uint32_t lo = off[r], hi2 = off[r + 1];  // block r: s_all[lo, hi2), descending
+      const uint32_t first = lo;
+      while (lo < hi2) {
+        const uint32_t mid = (lo + hi2) >> 1;
+        if (s_all[mid] > x) lo = mid + 1;
+        else hi2 = mid;
+      }
+      pos += lo - first;
+    }
+    if (pos < keff) {
+      st_stream_s32(out_ids + pos, static_cast<int32_t>(static_cast<uint32_t>(x & 0xFFFFFFFFull)));
+      st_stream_f32(out_scores + pos, key_to_float(static_cast<uint32_t>(x >> 32)));
+    }
+  }
+  if (rank == 0) {
+    for (uint32_t r = keff + tid; r < K; r += kMergeThreads) {  // fewer visible keys than top_k
+      st_stream_s32(out_ids + r, -1);
+      st_stream_f32(out_scores + r, -__int_as_float(0x7F800000));
+    }
+  }
 }
 
 }  // namespace itk

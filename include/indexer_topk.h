@@ -111,9 +111,10 @@ ITK_API size_t indexer_topk_workspace_bytes(itk_plan plan);
 /*
  * One scan on `stream`: two kernel launches -- the scan, which leaves each query's
  * candidates (a superset of its top-k, at most 4096 keys) in the workspace, then the
- * selection, which writes the sorted top-k rows -- with a third launch between them, the
- * merge of split queries, for split-tail descriptors (see indexer_topk_unit_table); plus a
- * 32-byte memset only right after a failed launch. Arguments:
+ * selection, which writes the sorted top-k rows. A split-tail descriptor (see
+ * indexer_topk_unit_table) adds the merge, which selects and writes the rows of its split
+ * queries from their chunks' candidates; the selection is left out when every query is
+ * split. Plus a 32-byte memset only right after a failed launch. Arguments:
  *   q          device, BF16 [T,H,D] row-major, 16-byte aligned
  *   k          device, BF16 [Tkv,D] row-major, 16-byte aligned
  *   w          device, FP32 [T,H] row-major
@@ -168,8 +169,8 @@ ITK_API int64_t indexer_topk_num_units(const itk_desc* desc);
  * causal position of the first query, first key tile, end key tile} -- the unit scans key
  * tiles [first, end) of 128 keys. A descriptor with at most 64 query blocks (a "split
  * tail") has every block of at least 8 visible key tiles split into consecutive units of
- * about 4 tiles (at most 256 units in all), whose candidates are merged per query before
- * the selection; otherwise a unit covers all visible tiles of its block. Writes min(capacity, n)
+ * about 4 tiles (at most 256 units in all), whose candidates are merged per query into
+ * its output row; otherwise a unit covers all visible tiles of its block. Writes min(capacity, n)
  * units to `units` (int32 [capacity][6]) and returns n, or -status on an invalid
  * descriptor. Reference: flashinfer PR #8691, benchmark rows A1-A3 ("split tail: 4
  * queries in one segment").
@@ -189,7 +190,7 @@ ITK_API const char* indexer_topk_version(void);
  * Scan without any device allocation: same operation, arguments and output as
  * indexer_topk_prepare + indexer_topk_run, but every byte of scratch (working buffers,
  * candidate store, work-unit table, ticket blocks, status word) lives in one static
- * device array of indexer_topk_noalloc_scratch_bytes() bytes (about 153 MB) that every
+ * device array of indexer_topk_noalloc_scratch_bytes() bytes (about 159 MB) that every
  * GPU loading this library holds until the process exits. The store holds 512 work units
  * (2048 queries); larger inputs run as one scan + selection launch pair per 512 units. The paper has no counterpart: it exists for
  * callers that must not call cudaMalloc at call time -- a serving runtime or framework
@@ -212,8 +213,8 @@ ITK_API int indexer_topk_run_noalloc(const itk_desc* desc, const void* q, const 
 /*
  * Per-kernel timing: from now on, every indexer_topk_run of this plan records `event` (a
  * cudaEvent_t owned by the caller, created on the plan's device) on the run's stream
- * between the scan launch and the selection launch, so that events recorded by the caller
- * before and after the run bracket each kernel. NULL stops the recording. Host only;
+ * right after the scan launch (before the merge and selection launches), so that events
+ * recorded by the caller before and after the run bracket the scan and the rest. NULL stops the recording. Host only;
  * returns ITK_ERR_INVALID_ARGUMENT for a NULL plan. Not part of the operation.
  */
 ITK_API int indexer_topk_set_split_event(itk_plan plan, void* event);

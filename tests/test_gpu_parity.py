@@ -194,7 +194,7 @@ def test_split_tail_matches_unsplit(binding, dev, oracle_mod, kind):
 
 
 def test_eager_matches_prepared_on_a_split_tail(binding, dev):
-    """The eager entry runs the same three launches (scan, merge, selection) for a split tail."""
+    """The eager entry runs the same launches (the scan, then the merge) for a split tail."""
     import torch
 
     wl = inputs.draw(8, 7000, [0, 8], [0, 7000], 300, seed=13, kind="normal")
