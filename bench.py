@@ -318,27 +318,34 @@ def _measure(binding, torch, wl, dev, steps, warmup, flush_buf):
     return plan, (q, k, w, ids, sc, ws), stream
 
 
-def _timed_steps(binding, torch, plan, bufs, stream, steps, flush_buf):
-    """Times `steps` runs with CUDA events on the launching stream: per step the whole call
-    (start..end) and, through the library's split event recorded between its two launches,
-    the scan kernel (start..split) and the selection kernel (split..end). The L2 is
-    flushed before every step, outside the events."""
+def _timed_steps(binding, torch, plan, bufs, stream, steps, flush_buf, split=False):
+    """Times `steps` runs with CUDA events on the launching stream, the L2 flushed before
+    every step outside the events. Without `split`: the whole call (start..end), launched
+    exactly as a caller launches it. With `split`: the library also records an event right
+    after the scan launch, so start..split is the scan kernel and split..end the rest. That
+    event sits between two kernels that otherwise overlap their launch (programmatic
+    dependent launch), so split runs serve the per-kernel figures only."""
     starts, splits, ends = ([torch.cuda.Event(enable_timing=True) for _ in range(steps)] for _ in range(3))
     for e in splits:  # create the events' device handles
         e.record(stream)
     torch.cuda.synchronize()
     for i in range(steps):
         flush_buf.fill_(i & 0xFF)
-        binding.indexer_topk_set_split_event(plan, splits[i])
+        if split:
+            binding.indexer_topk_set_split_event(plan, splits[i])
         starts[i].record(stream)
         binding.indexer_topk_run(plan, *bufs, stream)
         ends[i].record(stream)
-    binding.indexer_topk_set_split_event(plan, None)
-    return starts, splits, ends
+    if split:
+        binding.indexer_topk_set_split_event(plan, None)
+    return starts, (splits if split else None), ends
 
 
 def _step_ms(starts, splits, ends):
+    ends[-1].synchronize()
     total = np.array([a.elapsed_time(b) for a, b in zip(starts, ends)])
+    if splits is None:
+        return float(total.mean()), None, None
     scan = np.array([a.elapsed_time(b) for a, b in zip(starts, splits)])
     sel = np.array([a.elapsed_time(b) for a, b in zip(splits, ends)])
     return float(total.mean()), float(scan.mean()), float(sel.mean())
@@ -524,11 +531,17 @@ def run_ours(args):
     clocks.mark_timed(t_timed0, time.time())
     wall = time.perf_counter() - wall0
     plan.device_status()
-    total_ms, scan_ms, sel_ms = _step_ms(starts, splits, ends)
+    total_ms, _, _ = _step_ms(starts, splits, ends)
     ms = max_over_ranks(total_ms, dist, dev)
+    value = job_tflops(flops, world, ms)
+    # per-kernel figures: the same steps again with the split event between the launches
+    split_ms, scan_ms, sel_ms = _step_ms(*_timed_steps(binding, torch, plan, bufs, stream, args.steps, flush_buf,
+                                                       split=True))
+    torch.cuda.synchronize()
+    plan.device_status()
+    split_ms = max_over_ranks(split_ms, dist, dev)
     scan_ms = max_over_ranks(scan_ms, dist, dev)
     sel_ms = max_over_ranks(sel_ms, dist, dev)
-    value = job_tflops(flops, world, ms)
 
     # end to end through the public API with pinned host buffers
     e2e = None
@@ -541,10 +554,10 @@ def run_ours(args):
         wl2 = inputs.make(name, seed=rank)
         f2 = 2.0 * visible_pairs(wl2) * wl2.H * wl2.D
         plan2, b2, st2 = _measure(binding, torch, wl2, dev, args.steps, args.warmup, flush_buf)
-        s2, sp2, e2 = _timed_steps(binding, torch, plan2, b2, st2, args.steps, flush_buf)
+        m2, _, _ = _step_ms(*_timed_steps(binding, torch, plan2, b2, st2, args.steps, flush_buf))
+        _, m2_scan, m2_sel = _step_ms(*_timed_steps(binding, torch, plan2, b2, st2, args.steps, flush_buf, split=True))
         torch.cuda.synchronize()
         plan2.device_status()
-        m2, m2_scan, m2_sel = _step_ms(s2, sp2, e2)
         tf2 = f2 / (m2 * 1e-3) / 1e12
         tf2_scan = f2 / (m2_scan * 1e-3) / 1e12
         per_config[name] = {"ms": m2, "tflops": tf2, "frac": tf2 / peaks["bf16_tflops"],
@@ -581,7 +594,9 @@ def run_ours(args):
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(),
         "gpu_launches": (1 + len(finish)) * args.steps,
         "kernels": {"indexer_topk_scan_kernel": {"ms": scan_ms, "launches": args.steps},
-                    " + ".join(f"indexer_topk_{f}_kernel" for f in finish): {"ms": sel_ms, "launches": args.steps}},
+                    " + ".join(f"indexer_topk_{f}_kernel" for f in finish): {"ms": sel_ms, "launches": args.steps},
+                    "split_run_ms_per_step": split_ms,
+                    "note": "separate runs of the same steps with an event between the launches"},
         "per_config": per_config, "wall_s_timed_region": wall,
     }
     print(json.dumps(line), flush=True)

@@ -16,6 +16,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "../../include/indexer_topk.h"
@@ -298,6 +299,27 @@ int ensure_kernel_attributes() {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Launches `kernel` on `stream` as a programmatic dependent of the stream's previous kernel:
+// its CTAs may start (and run their set-up) while that kernel's last CTAs finish; each
+// kernel waits (griddepcontrol.wait) before it reads anything the previous one wrote.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), int grid, int block, size_t smem, cudaStream_t stream,
+                             Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(block));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  const cudaError_t last = cudaGetLastError();  // clears the launch error, as after a <<<>>> launch
+  return e != cudaSuccess ? e : last;
+}
+
 int check_run_buffers(const Layout& L, const void* q, const void* k, const float* w, int32_t* ids, float* scores) {
   if (!q || !k || !w || !ids || !scores) return fail(ITK_ERR_NULL_POINTER, "q, k, w, out_ids or out_scores is NULL");
   if (!aligned(q, 16) || !aligned(k, 16)) return fail(ITK_ERR_MISALIGNED, "q and k must be 16-byte aligned");
@@ -336,8 +358,7 @@ int launch_run(const Layout& L, int grid, int sm_count, const RunTables& t, cons
   // A test hook asks for a launch the runtime must refuse: a dynamic shared-memory request
   // above the device limit is rejected at launch time and no work reaches the GPU.
   const size_t smem = force_launch_failure ? size_t(1) << 30 : itk::kSmemBytes;
-  itk::indexer_topk_scan_kernel<<<grid, itk::kNumThreads, smem, stream>>>(qmap, kmap, prm);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent(itk::indexer_topk_scan_kernel, grid, itk::kNumThreads, smem, stream, qmap, kmap, prm);
   if (e != cudaSuccess) return cuda_fail(e, "scan launch");
   if (split_event) {
     e = cudaEventRecord(split_event, stream);
@@ -353,9 +374,8 @@ int launch_run(const Layout& L, int grid, int sm_count, const RunTables& t, cons
     mp.status = t.status;
     mp.out_ids = ids;
     mp.out_scores = scores;
-    itk::indexer_topk_merge_kernel<<<static_cast<int>(t.n_merges) * itk::kMergeCluster, itk::kMergeThreads,
-                                     itk::kMergeSmemBytes, stream>>>(mp);
-    e = cudaGetLastError();
+    e = launch_dependent(itk::indexer_topk_merge_kernel, static_cast<int>(t.n_merges) * itk::kMergeCluster,
+                         itk::kMergeThreads, itk::kMergeSmemBytes, stream, mp);
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   }
   if (!t.select) return ITK_OK;
@@ -372,8 +392,7 @@ int launch_run(const Layout& L, int grid, int sm_count, const RunTables& t, cons
   const size_t items = t.n_slots;
   const int sel_grid = static_cast<int>(
       std::max<size_t>(1, std::min<size_t>(static_cast<size_t>(sm_count), (items + itk::kSelGroups - 1) / itk::kSelGroups)));
-  itk::indexer_topk_select_kernel<<<sel_grid, itk::kSelThreads, kSelSmemLaunch, stream>>>(sp);
-  e = cudaGetLastError();
+  e = launch_dependent(itk::indexer_topk_select_kernel, sel_grid, itk::kSelThreads, kSelSmemLaunch, stream, sp);
   if (e != cudaSuccess) return cuda_fail(e, "selection launch");
   return ITK_OK;
 }

@@ -372,6 +372,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *s_tmem;
+  grid_dep_wait();  // the kernel that wrote q, k and w (if launched as its dependent) is complete
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -401,7 +402,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         s_unit[2 * slot] = unit;
         s_unit[2 * slot + 1] = range;  // unit index, key tiles [tile0, tile1)
         mbar_arrive(bars.uf(slot));
-        if (unit.x < 0) break;
+        if (unit.x < 0) {
+          grid_dep_launch_dependents();  // no unit left for this CTA: the next kernel may launch
+          break;
+        }
         if (!mbar_wait(bars.qempty, (it & 1) ^ 1, s_abort)) {
           record_timeout(p.status, s_abort, 2);
           break;

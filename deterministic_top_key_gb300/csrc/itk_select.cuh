@@ -304,6 +304,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) indexer_topk_select_kernel(con
   uint32_t* flags = reinterpret_cast<uint32_t*>(gs + kSgFlags);
   volatile unsigned long long* s_item = reinterpret_cast<volatile unsigned long long*>(gs + kSgItem);
   const unsigned long long n_items = static_cast<unsigned long long>(p.n_items);
+  grid_dep_wait();  // the scan (and merge) that wrote the candidates is complete
 
   while (true) {
     if (c.gtid == 0) *s_item = atomicAdd(&p.ticket->next, 1ull);
@@ -449,6 +450,7 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __launch_bounds__(kMergeTh
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
   const MergeDesc m = p.merges[blockIdx.x / kMergeCluster];
+  grid_dep_wait();  // the scan that wrote the chunks' candidates is complete
   int n_chunks = m.n_chunks;
   if (n_chunks > kMaxMergeChunks) {  // the host never builds one; keep the walk in bounds
     if (rank == 0 && tid == 0) atomicOr(p.status, kStatusInternal | (21u << 8));
