@@ -16,9 +16,11 @@
 // positions are kept, and each kept bin b with c_b keys is spread over c_b sub-buckets by
 // linear position inside the bin, so sub-buckets hold about one key each. Counting, a
 // prefix sum and a scatter put every key into its sub-bucket's slot range, in descending
-// order of sub-bucket; sorting each (tiny) sub-bucket in place finishes the order. Two
-// exact fallbacks handle heavy ties: a radix select inside an oversized sub-bucket that
-// crosses position top_k, and a full bitonic sort when some sub-bucket is large.
+// order of sub-bucket; a key's place in the row is then its sub-bucket's start plus the
+// number of keys above it in the same (tiny) sub-bucket, and it is written there
+// directly. Heavy ties take exact fallbacks: in-place sorts of the sub-buckets, a radix
+// select inside an oversized sub-bucket that crosses position top_k, and a full bitonic
+// sort when some sub-bucket is large.
 #pragma once
 
 #include "itk_common.cuh"
@@ -41,7 +43,8 @@ constexpr uint32_t kSgRadix = kSgStage + (kMaxTopK + kStageSlack) * 8; // 256 x 
 constexpr uint32_t kSgSel = kSgRadix + 256 * 4;                        // 8 x u32
 constexpr uint32_t kSgFlags = kSgSel + 8 * 4;                          // 4 x u32
 constexpr uint32_t kSgItem = kSgFlags + 4 * 4;                         // 4 x u32 (drawn item)
-constexpr uint32_t kSgBytes = (kSgItem + 16 + 127) / 128 * 128;
+constexpr uint32_t kSgBkt = kSgItem + 16;                              // (2048 + 256) x u16: sub-bucket of each staged key
+constexpr uint32_t kSgBytes = (kSgBkt + (kMaxTopK + kStageSlack) * 2 + 127) / 128 * 128;
 constexpr uint32_t kSelSmemBytes = kSelGroups * kSgBytes;
 static_assert(kSgStage % 16 == 0, "alignment");
 static_assert(kSelSmemBytes <= 232448, "shared memory budget");
@@ -152,7 +155,7 @@ __device__ __noinline__ void sel_crossing_fallback(const GroupCtx& c, const unsi
 // place them.
 __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned long long* buf, uint32_t n,
                                            uint32_t top_k, uint32_t* ge, uint32_t* sub, unsigned long long* stage,
-                                           uint32_t* flags, int32_t* out_ids, float* out_scores) {
+                                           uint16_t* bkt, uint32_t* flags, int32_t* out_ids, float* out_scores) {
   const uint32_t* buf_hi = reinterpret_cast<const uint32_t*>(buf) + 1;  // high word of entry i at buf_hi[2 i]
   uint32_t hk[kPerThread];
   uint32_t valid = 0;
@@ -225,13 +228,52 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
 #pragma unroll
   for (int r = 0; r < kPerThread; ++r) {
     if ((kept >> r) & 1u) {
-      const uint32_t pos = atomicAdd(&sub[sub_pad(sub_bucket(ge, hk[r]))], 1u);
-      if (pos < cap) stage[pos] = buf[c.gtid + 128u * r];
+      const uint32_t b = sub_bucket(ge, hk[r]);
+      const uint32_t pos = atomicAdd(&sub[sub_pad(b)], 1u);
+      if (pos < cap) {
+        stage[pos] = buf[c.gtid + 128u * r];
+        bkt[pos] = static_cast<uint16_t>(b);
+      }
     }
   }
   gsync(c);
-  // sub(i) is now the end of sub-bucket i; sort every sub-bucket that reaches a slot below
-  // top_k, in place (they hold about one key each)
+  // sub(i) is now the end of sub-bucket i. Common case: every sub-bucket that reaches a
+  // slot below keff is small and inside the staging area; each staged key's position is
+  // then its sub-bucket's start plus the number of keys above it in that sub-bucket.
+  for (uint32_t i = c.gtid; i < m_keep; i += 128) {
+    const uint32_t start = i ? sub[sub_pad(i - 1)] : 0u;
+    const uint32_t end = sub[sub_pad(i)];
+    if (start >= keff || end - start < 2) continue;
+    if (end - start > static_cast<uint32_t>(kBigBucket) || (end > keff && end > cap)) flags[1] = 1u;
+  }
+  gsync(c);
+  if (flags[1] == 0u) {  // uniform: read by every thread before anyone writes it again
+    const uint32_t staged = m_keep < cap ? m_keep : cap;
+    for (uint32_t j = c.gtid; j < staged; j += 128) {
+      const uint32_t b = bkt[j];
+      const uint32_t start = b ? sub[sub_pad(b - 1)] : 0u;
+      if (start >= keff) continue;
+      const uint32_t end = sub[sub_pad(b)];
+      const unsigned long long x = stage[j];
+      uint32_t pos = start;
+      for (uint32_t i = start; i < end; ++i) pos += stage[i] > x ? 1u : 0u;
+      if (pos < keff) {
+        st_stream_s32(out_ids + pos, static_cast<int32_t>(static_cast<uint32_t>(x & 0xFFFFFFFFull)));
+        st_stream_f32(out_scores + pos, key_to_float(static_cast<uint32_t>(x >> 32)));
+      }
+    }
+    for (uint32_t r = keff + c.gtid; r < top_k; r += 128) {
+      st_stream_s32(out_ids + r, -1);
+      st_stream_f32(out_scores + r, -__int_as_float(0x7F800000));
+    }
+    gsync(c);
+    return;
+  }
+  gsync(c);  // every thread has read flags[1]
+  if (c.gtid == 0) flags[1] = 0u;
+  gsync(c);
+  // Heavy ties: sort every sub-bucket that reaches a slot below top_k in place, resolve
+  // an oversized crossing sub-bucket exactly, and sort the whole range when needed.
   for (uint32_t i = c.gtid; i < m_keep; i += 128) {
     const uint32_t start = i ? sub[sub_pad(i - 1)] : 0u;
     const uint32_t end = sub[sub_pad(i)];
@@ -301,6 +343,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) indexer_topk_select_kernel(con
   uint32_t* ge = reinterpret_cast<uint32_t*>(gs + kSgBins);
   uint32_t* sub = reinterpret_cast<uint32_t*>(gs + kSgSub);
   unsigned long long* stage = reinterpret_cast<unsigned long long*>(gs + kSgStage);
+  uint16_t* bkt = reinterpret_cast<uint16_t*>(gs + kSgBkt);
   uint32_t* flags = reinterpret_cast<uint32_t*>(gs + kSgFlags);
   volatile unsigned long long* s_item = reinterpret_cast<volatile unsigned long long*>(gs + kSgItem);
   const unsigned long long n_items = static_cast<unsigned long long>(p.n_items);
@@ -320,7 +363,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) indexer_topk_select_kernel(con
       if (c.gtid == 0) atomicOr(p.status, kStatusInternal | (20u << 8));
       n = kCap;
     }
-    sel_finish(c, p.store + item * kCap, n, static_cast<uint32_t>(p.top_k), ge, sub, stage, flags,
+    sel_finish(c, p.store + item * kCap, n, static_cast<uint32_t>(p.top_k), ge, sub, stage, bkt, flags,
                p.out_ids + row * p.top_k, p.out_scores + row * p.top_k);
   }
   __syncthreads();
