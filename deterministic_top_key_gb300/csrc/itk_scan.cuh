@@ -584,6 +584,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t x[32];
             tmem_ld32(lane_addr + col + 32 * half, x);
             tmem_ld_wait();
+            if (half == 1) {  // every column is in registers: hand the accumulator back now
+              tc_fence_before_sync();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bars.ae(ab));
+            }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {  // heads 32 half + 8i .. + 7
               const float4 wa = wv[8 * half + 2 * i];
@@ -604,10 +609,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           score = (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]))) + 0.0f;
         }
-        // the accumulator buffer is read: hand it back to the MMA
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.ae(ab));
+        if (!active) {  // this group reads no columns of the buffer
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars.ae(ab));
+        }
         // append the keys that pass the filter
         const bool ins = active && jl <= last_key && score >= thr_f;  // == bin(score) >= thr for finite scores
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, ins);
