@@ -132,19 +132,30 @@ __device__ __forceinline__ uint32_t hist_get(const uint32_t* h, uint32_t b) { re
 __device__ __forceinline__ void hist_inc(uint32_t* h, uint32_t b) { atomicAdd(&h[b], 1u); }
 
 // Radix select streamed from global memory, one byte per pass: returns `prefix` with
-// #{x in buf[0..n) : x >= prefix} == K (K <= n, keys distinct). Used only when ties crowd
-// one histogram bin, so speed matters little.
+// #{x in buf[0..n) : x >= prefix} == K (K <= n, keys distinct). Used when the score bin at
+// the threshold is crowded (more than kCap keys at or above it at a hand-off, or a
+// compaction that cannot drop enough).
 __device__ __noinline__ unsigned long long group_select_stream(const GroupCtx& c, const unsigned long long* buf,
                                                                uint32_t n, uint32_t K) {
+  constexpr int kChunk = 8;  // keys a thread loads before counting them
   unsigned long long prefix = 0ull;
   uint32_t k_rem = K;
   for (int shift = 56; shift >= 0; shift -= 8) {
     for (int i = c.gtid; i < 256; i += 128) c.radix[i] = 0u;
     gsync(c);
     const unsigned long long hi_mask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
-    for (uint32_t i = c.gtid; i < n; i += 128) {
-      const unsigned long long x = buf[i];
-      if ((x & hi_mask) == (prefix & hi_mask)) atomicAdd(&c.radix[(x >> shift) & 0xFFu], 1u);
+    for (uint32_t base = 0; base < n; base += 128 * kChunk) {
+      unsigned long long x[kChunk];
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r) {
+        const uint32_t idx = base + c.gtid + 128u * r;
+        x[r] = idx < n ? buf[idx] : 0ull;
+      }
+#pragma unroll
+      for (int r = 0; r < kChunk; ++r) {
+        const uint32_t idx = base + c.gtid + 128u * r;
+        if (idx < n && (x[r] & hi_mask) == (prefix & hi_mask)) atomicAdd(&c.radix[(x[r] >> shift) & 0xFFu], 1u);
+      }
     }
     gsync(c);
     group_pick_digit(c, k_rem);
@@ -158,25 +169,66 @@ __device__ __noinline__ unsigned long long group_select_stream(const GroupCtx& c
   return prefix;
 }
 
-// Appends the keys of buf[0..n) at or above `prefix` to dst[0..limit) through the group
-// cursor *s_cursor (reset here); returns the number appended.
+// Copies the keys x of buf[0..n) with keep(x) to dst[0..limit) (dst may be buf itself:
+// every key of a chunk is read before any slot of it is rewritten, and no more keys are
+// kept than read); returns the number that qualified. A thread loads kChunk keys, then
+// writes its kept ones to consecutive slots; a warp reserves its slots with one atomic.
+template <typename Keep>
+__device__ __forceinline__ uint32_t group_copy_if(const GroupCtx& c, const unsigned long long* buf, uint32_t n,
+                                                  Keep keep, unsigned long long* dst, uint32_t limit, uint32_t* s_pos,
+                                                  uint64_t pol_src, uint64_t pol_dst) {
+  constexpr int kChunk = 16;  // keys per thread per pass
+  if (c.gtid == 0) *s_pos = 0u;
+  gsync(c);
+  for (uint32_t base = 0; base < n; base += 128 * kChunk) {
+    unsigned long long x[kChunk];
+#pragma unroll
+    for (int r = 0; r < kChunk; ++r) {
+      const uint32_t idx = base + c.gtid + 128u * r;
+      x[r] = idx < n ? ld_hint_u64(buf + idx, pol_src) : 0ull;
+    }
+    gsync(c);
+    uint32_t km = 0;
+#pragma unroll
+    for (int r = 0; r < kChunk; ++r) {
+      const uint32_t idx = base + c.gtid + 128u * r;
+      km |= (idx < n && keep(x[r]) ? 1u : 0u) << r;
+    }
+    const uint32_t cnt = static_cast<uint32_t>(__popc(km));
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (c.lane >= off) incl += t;
+    }
+    uint32_t wbase = 0;
+    if (c.lane == 31 && incl) wbase = atomicAdd(s_pos, incl);
+    wbase = __shfl_sync(0xFFFFFFFFu, wbase, 31);
+    uint32_t pos = wbase + incl - cnt;
+#pragma unroll
+    for (int r = 0; r < kChunk; ++r) {
+      if ((km >> r) & 1u) {
+        if (pos < limit) st_hint_u64(dst + pos, x[r], pol_dst);
+        ++pos;
+      }
+    }
+  }
+  gsync(c);
+  const uint32_t m = *s_pos;
+  gsync(c);
+  return m;
+}
+
+// Appends the keys of buf[0..n) at or above `prefix` to dst[0..limit); returns the number
+// appended.
 __device__ __forceinline__ uint32_t group_keep_at_or_above(const GroupCtx& c, const unsigned long long* buf,
                                                            uint32_t n, unsigned long long prefix,
                                                            unsigned long long* dst, uint32_t limit,
                                                            uint32_t* s_cursor) {
-  if (c.gtid == 0) *s_cursor = 0u;
-  gsync(c);
-  for (uint32_t base = 0; base < n; base += 128) {
-    const uint32_t i = base + c.gtid;
-    const unsigned long long x = i < n ? buf[i] : 0ull;
-    const bool keep = i < n && x >= prefix;
-    const uint32_t slot = warp_append_slot(keep, s_cursor, c.lane);
-    if (keep && slot < limit) dst[slot] = x;  // exactly `limit` keys qualify: keys are distinct
-  }
-  gsync(c);
-  const uint32_t m = *s_cursor;
-  gsync(c);
-  return m < limit ? m : limit;
+  const uint64_t pol = policy_evict_last();
+  const uint32_t m = group_copy_if(c, buf, n, [prefix](unsigned long long x) { return x >= prefix; }, dst, limit,
+                                   s_cursor, pol, pol);
+  return m < limit ? m : limit;  // exactly `limit` keys qualify: keys are distinct
 }
 
 // Keeps exactly the K largest of the n keys in buf (n > K): they go through `scratch`
@@ -196,34 +248,12 @@ __device__ uint32_t group_exact_in_place(const GroupCtx& c, unsigned long long* 
 }
 
 // Drops the keys of buf[0..n) whose bin is below thr, writing the survivors to dst[0..limit)
-// (dst may be buf itself: every key of a chunk is read before any slot of it is
-// rewritten); returns the number that qualified (callers make sure it is <= limit).
+// (dst may be buf itself); returns the number that qualified (callers make sure it is <= limit).
 __device__ __forceinline__ uint32_t group_drop_below(const GroupCtx& c, unsigned long long* buf, uint32_t n,
                                                      uint32_t thr, unsigned long long* dst, uint32_t limit,
                                                      uint32_t* s_pos, uint64_t pol_src, uint64_t pol_dst) {
-  constexpr int kChunk = 16;  // keys per thread per pass
-  if (c.gtid == 0) *s_pos = 0u;
-  gsync(c);
-  for (uint32_t base = 0; base < n; base += 128 * kChunk) {
-    unsigned long long x[kChunk];
-#pragma unroll
-    for (int r = 0; r < kChunk; ++r) {
-      const uint32_t idx = base + c.gtid + 128u * r;
-      x[r] = idx < n ? ld_hint_u64(buf + idx, pol_src) : 0ull;
-    }
-    gsync(c);
-#pragma unroll
-    for (int r = 0; r < kChunk; ++r) {
-      const uint32_t idx = base + c.gtid + 128u * r;
-      const bool keep = idx < n && bin_of(x[r]) >= thr;
-      const uint32_t slot = warp_append_slot(keep, s_pos, c.lane);
-      if (keep && slot < limit) st_hint_u64(dst + slot, x[r], pol_dst);
-    }
-  }
-  gsync(c);
-  const uint32_t m = *s_pos;
-  gsync(c);
-  return m;
+  return group_copy_if(c, buf, n, [thr](unsigned long long x) { return bin_of(x) >= thr; }, dst, limit, s_pos,
+                       pol_src, pol_dst);
 }
 
 // Mid-unit compaction of one working buffer, so that at most `limit` keys remain: drops
