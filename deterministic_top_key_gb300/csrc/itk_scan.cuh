@@ -38,8 +38,12 @@
 // keys. It only rises, and every key it rejects is below top_k keys already seen, so the
 // buffer always contains the exact top-k of the keys seen so far. The filter compares
 // the score itself with the lowest score of the threshold bin, and forms the 64-bit key
-// only for the keys it appends.
+// only for the keys it appends. A unit whose queries see at most kCap keys of its tile
+// range skips the filter: every visible key goes straight to the store slot (no
+// histogram, no sync points, no hand-off copy); the tile loop is compiled for both cases.
 #pragma once
+
+#include <type_traits>
 
 #include "itk_common.cuh"
 
@@ -568,106 +572,123 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int4 range = s_unit[2 * slot + 1];
       const size_t uidx = static_cast<size_t>(range.x);
       if (c.gtid < kHeads) s_w[g * kHeads + c.gtid] = active ? p.w[static_cast<size_t>(unit.x + g) * kHeads + c.gtid] : 0.f;
-      for (int i = c.gtid; i < kBins; i += 128) hist_g[i] = 0u;
+      // A unit whose queries see at most kCap keys of its tile range hands every visible
+      // key over: the appends go straight to the store slots, with no histogram, no sync
+      // points and no copy at the end (uniform across the CTA).
+      const bool direct = min(unit.w + unit.y, range.z * kBlockKeys) - range.y * kBlockKeys <= kCap;
+      if (!direct)
+        for (int i = c.gtid; i < kBins; i += 128) hist_g[i] = 0u;
       if (c.gtid < 4) qs[c.gtid] = 0u;
       gsync(c);
       const int tile0 = range.y, nt = range.z - range.y;
       const int last_key = unit.w + g;  // causal bound: local keys 0..last_key are visible
-      bool failed = false;
-      uint32_t thr = 0u;  // threshold bin, refreshed at every sync point
-      float thr_f = -__int_as_float(0x7F800000);  // the lowest score of bin thr (bins below 4 hold no finite score)
-      for (int tile = 0; tile < nt; ++tile, ++ac) {
-        const int ab = ac & 1;
-        if (tile % kSyncEvery == sync_phase) {
-          // Group sync point (the only barriers inside a unit): every append of the
-          // earlier tiles is done, so the count and the histogram are final.
-          gsync(c);
-          if (s_gfail[g]) {  // uniform: read after the barrier
-            failed = true;
-            break;
-          }
-          if (active) {
-            if (c.gwarp == 0) warp_raise_threshold(qs, hist_g, K, lane);
+      // The tile loop, compiled once for direct units and once for the others.
+      auto scan_tiles = [&](auto direct_tag) -> bool {
+        constexpr bool kDirect = decltype(direct_tag)::value;
+        unsigned long long* app = kDirect ? p.store + (uidx * kQB + g) * kCap : cand;
+        const uint64_t pol_app = kDirect ? pol_store : pol_cand;
+        bool failed = false;
+        uint32_t thr = 0u;  // threshold bin, refreshed at every sync point
+        float thr_f = -__int_as_float(0x7F800000);  // the lowest score of bin thr (bins below 4 hold no finite score)
+        for (int tile = 0; tile < nt; ++tile, ++ac) {
+          const int ab = ac & 1;
+          if (!kDirect && tile % kSyncEvery == sync_phase) {
+            // Group sync point (the only barriers inside a unit): every append of the
+            // earlier tiles is done, so the count and the histogram are final.
             gsync(c);
-            // make room for the appends of the next kSyncEvery tiles (uniform decision)
-            if (qs[0] > kCompactAt)
-              epi_compact(c, cand, qs, hist_g, K, &s_pos[g], pol_cand, kCompactAt, exact_scratch);
-            thr = qs[2];
-            thr_f = thr < 4u ? -__int_as_float(0x7F800000) : key_to_float(thr << kBinShift);
-          }
-        }
-        if (!mbar_wait(bars.af(ab), (ac >> 1) & 1, s_abort)) {
-          record_timeout(p.status, s_abort, 10);
-          atomicOr(&s_gfail[g], 1u);  // the group leaves at its next sync point
-          continue;
-        }
-        tc_fence_after_sync();
-        const int jl = (tile0 + tile) * kBlockKeys + key_lane;  // local key index within the segment
-        float score = 0.f;
-        if (active) {
-          const uint32_t col = static_cast<uint32_t>(ab * kN + g * kHeads);
-          float ps[8];
-#pragma unroll
-          for (int m = 0; m < 8; ++m) ps[m] = 0.f;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {  // heads 32 half .. 32 half + 31
-            uint32_t x[32];
-            tmem_ld32(lane_addr + col + 32 * half, x);
-            tmem_ld_wait();
-            if (half == 1) {  // every column is in registers: hand the accumulator back now
-              tc_fence_before_sync();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bars.ae(ab));
+            if (s_gfail[g]) {  // uniform: read after the barrier
+              failed = true;
+              break;
             }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {  // heads 32 half + 8i .. + 7
-              const float4 wa = wv[8 * half + 2 * i];
-              const float4 wb = wv[8 * half + 2 * i + 1];
-              const float r0 = fmaxf(__uint_as_float(x[8 * i + 0]), 0.f);
-              const float r1 = fmaxf(__uint_as_float(x[8 * i + 1]), 0.f);
-              const float r2 = fmaxf(__uint_as_float(x[8 * i + 2]), 0.f);
-              const float r3 = fmaxf(__uint_as_float(x[8 * i + 3]), 0.f);
-              const float r4 = fmaxf(__uint_as_float(x[8 * i + 4]), 0.f);
-              const float r5 = fmaxf(__uint_as_float(x[8 * i + 5]), 0.f);
-              const float r6 = fmaxf(__uint_as_float(x[8 * i + 6]), 0.f);
-              const float r7 = fmaxf(__uint_as_float(x[8 * i + 7]), 0.f);
-              ffma2(ps[0], ps[1], wa.x, wa.y, r0, r1);
-              ffma2(ps[2], ps[3], wa.z, wa.w, r2, r3);
-              ffma2(ps[4], ps[5], wb.x, wb.y, r4, r5);
-              ffma2(ps[6], ps[7], wb.z, wb.w, r6, r7);
+            if (active) {
+              if (c.gwarp == 0) warp_raise_threshold(qs, hist_g, K, lane);
+              gsync(c);
+              // make room for the appends of the next kSyncEvery tiles (uniform decision)
+              if (qs[0] > kCompactAt)
+                epi_compact(c, cand, qs, hist_g, K, &s_pos[g], pol_cand, kCompactAt, exact_scratch);
+              thr = qs[2];
+              thr_f = thr < 4u ? -__int_as_float(0x7F800000) : key_to_float(thr << kBinShift);
             }
           }
-          score = (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]))) + 0.0f;
-        }
-        if (!active) {  // this group reads no columns of the buffer
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bars.ae(ab));
-        }
-        // append the keys that pass the filter
-        const bool ins = active && jl <= last_key && score >= thr_f;  // == bin(score) >= thr for finite scores
-        const uint32_t m = __ballot_sync(0xFFFFFFFFu, ins);
-        if (m) {
-          const int lead = __ffs(m) - 1;
-          uint32_t base = 0u;
-          if (lane == lead) base = atomicAdd(&qs[0], static_cast<uint32_t>(__popc(m)));
-          base = __shfl_sync(0xFFFFFFFFu, base, lead);
-          if (ins) {
-            const uint32_t key32 = ord_key(score);
-            st_hint_u64(cand + base + __popc(m & ((1u << lane) - 1u)),
-                        (static_cast<unsigned long long>(key32) << 32) | static_cast<uint32_t>(unit.z + jl), pol_cand);
-            hist_inc(hist_g, key32 >> kBinShift);
+          if (!mbar_wait(bars.af(ab), (ac >> 1) & 1, s_abort)) {
+            record_timeout(p.status, s_abort, 10);
+            atomicOr(&s_gfail[g], 1u);  // the group leaves at its next sync point
+            continue;
+          }
+          tc_fence_after_sync();
+          const int jl = (tile0 + tile) * kBlockKeys + key_lane;  // local key index within the segment
+          float score = 0.f;
+          if (active) {
+            const uint32_t col = static_cast<uint32_t>(ab * kN + g * kHeads);
+            float ps[8];
+  #pragma unroll
+            for (int m = 0; m < 8; ++m) ps[m] = 0.f;
+  #pragma unroll
+            for (int half = 0; half < 2; ++half) {  // heads 32 half .. 32 half + 31
+              uint32_t x[32];
+              tmem_ld32(lane_addr + col + 32 * half, x);
+              tmem_ld_wait();
+              if (half == 1) {  // every column is in registers: hand the accumulator back now
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.ae(ab));
+              }
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) {  // heads 32 half + 8i .. + 7
+                const float4 wa = wv[8 * half + 2 * i];
+                const float4 wb = wv[8 * half + 2 * i + 1];
+                const float r0 = fmaxf(__uint_as_float(x[8 * i + 0]), 0.f);
+                const float r1 = fmaxf(__uint_as_float(x[8 * i + 1]), 0.f);
+                const float r2 = fmaxf(__uint_as_float(x[8 * i + 2]), 0.f);
+                const float r3 = fmaxf(__uint_as_float(x[8 * i + 3]), 0.f);
+                const float r4 = fmaxf(__uint_as_float(x[8 * i + 4]), 0.f);
+                const float r5 = fmaxf(__uint_as_float(x[8 * i + 5]), 0.f);
+                const float r6 = fmaxf(__uint_as_float(x[8 * i + 6]), 0.f);
+                const float r7 = fmaxf(__uint_as_float(x[8 * i + 7]), 0.f);
+                ffma2(ps[0], ps[1], wa.x, wa.y, r0, r1);
+                ffma2(ps[2], ps[3], wa.z, wa.w, r2, r3);
+                ffma2(ps[4], ps[5], wb.x, wb.y, r4, r5);
+                ffma2(ps[6], ps[7], wb.z, wb.w, r6, r7);
+              }
+            }
+            score = (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]))) + 0.0f;
+          }
+          if (!active) {  // this group reads no columns of the buffer
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.ae(ab));
+          }
+          // append the keys that pass the filter
+          const bool ins = active && jl <= last_key && score >= thr_f;  // == bin(score) >= thr for finite scores
+          const uint32_t m = __ballot_sync(0xFFFFFFFFu, ins);
+          if (m) {
+            const int lead = __ffs(m) - 1;
+            uint32_t base = 0u;
+            if (lane == lead) base = atomicAdd(&qs[0], static_cast<uint32_t>(__popc(m)));
+            base = __shfl_sync(0xFFFFFFFFu, base, lead);
+            if (ins) {
+              const uint32_t key32 = ord_key(score);
+              st_hint_u64(app + base + __popc(m & ((1u << lane) - 1u)),
+                          (static_cast<unsigned long long>(key32) << 32) | static_cast<uint32_t>(unit.z + jl), pol_app);
+              if (!kDirect) hist_inc(hist_g, key32 >> kBinShift);
+            }
           }
         }
-      }
+        return failed;
+      };
+      const bool failed = direct ? scan_tiles(std::true_type{}) : scan_tiles(std::false_type{});
       if (failed) break;
       // Hand-off: every candidate of the unit's query goes to the store.
       gsync(c);  // every append of the unit is done
       if (active) {
-        if (c.gwarp == 0) warp_raise_threshold(qs, hist_g, K, lane);
-        gsync(c);
         const size_t item = uidx * kQB + g;
-        epi_handoff(c, cand, qs, K, &s_pos[g], pol_cand, pol_store, p.store + item * kCap, p.counts + item, p.status);
+        if (direct) {
+          if (c.gtid == 0) p.counts[item] = qs[0];  // every visible key, at most kCap
+        } else {
+          if (c.gwarp == 0) warp_raise_threshold(qs, hist_g, K, lane);
+          gsync(c);
+          epi_handoff(c, cand, qs, K, &s_pos[g], pol_cand, pol_store, p.store + item * kCap, p.counts + item, p.status);
+        }
       }
       gsync(c);
       __syncwarp();
