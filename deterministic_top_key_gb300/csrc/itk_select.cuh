@@ -158,12 +158,19 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
                                            uint16_t* bkt, uint32_t* flags, int32_t* out_ids, float* out_scores) {
   const uint32_t* buf_hi = reinterpret_cast<const uint32_t*>(buf) + 1;  // high word of entry i at buf_hi[2 i]
   uint32_t hk[kPerThread];
-  uint32_t valid = 0;
+  // entry r of this thread is candidate gtid + 128 r: it exists for r < ceil((n - gtid) / 128)
+  const uint32_t n_mine = n > static_cast<uint32_t>(c.gtid) ? (n - c.gtid + 127u) / 128u : 0u;
+  const uint32_t valid = n_mine >= 32u ? 0xFFFFFFFFu : (1u << n_mine) - 1u;
 #pragma unroll
-  for (int r = 0; r < kPerThread; ++r) {
-    const uint32_t idx = c.gtid + 128u * r;
-    hk[r] = idx < n ? buf_hi[2 * idx] : 0u;
-    valid |= (idx < n ? 1u : 0u) << r;
+  for (int r = 0; r < kPerThread; ++r) hk[r] = 0u;
+#pragma unroll
+  for (int r0 = 0; r0 < kPerThread; r0 += 8) {  // runs of 8 entries with no bit set are skipped
+    if (((valid >> r0) & 0xFFu) == 0u) continue;
+#pragma unroll
+    for (int r = r0; r < r0 + 8; ++r) {
+      if (!((valid >> r) & 1u)) continue;
+      hk[r] = buf_hi[2 * (c.gtid + 128u * r)];
+    }
   }
   const uint32_t keff = n < top_k ? n : top_k;
   // count the candidates per bin
@@ -175,8 +182,14 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   }
   gsync(c);
 #pragma unroll
-  for (int r = 0; r < kPerThread; ++r)
-    if ((valid >> r) & 1u) atomicAdd(&ge[bin_pad(hk[r] >> kBinShift)], 1u);
+  for (int r0 = 0; r0 < kPerThread; r0 += 8) {  // runs of 8 entries with no bit set are skipped
+    if (((valid >> r0) & 0xFFu) == 0u) continue;
+#pragma unroll
+    for (int r = r0; r < r0 + 8; ++r) {
+      if (!((valid >> r) & 1u)) continue;
+      atomicAdd(&ge[bin_pad(hk[r] >> kBinShift)], 1u);
+    }
+  }
   gsync(c);
   // ge(b) = candidates in bins >= b (suffix sums, 16 bins per thread, highest bins first)
   {
@@ -216,18 +229,26 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   gsync(c);
   uint32_t kept = 0;  // bit r: candidate r lies in a kept bin
 #pragma unroll
-  for (int r = 0; r < kPerThread; ++r) {
-    if (((valid >> r) & 1u) && (hk[r] >> kBinShift) >= tstar) {
-      kept |= 1u << r;
-      atomicAdd(&sub[sub_pad(sub_bucket(ge, hk[r]))], 1u);
+  for (int r0 = 0; r0 < kPerThread; r0 += 8) {  // runs of 8 entries with no bit set are skipped
+    if (((valid >> r0) & 0xFFu) == 0u) continue;
+#pragma unroll
+    for (int r = r0; r < r0 + 8; ++r) {
+      if (!((valid >> r) & 1u)) continue;
+      if ((hk[r] >> kBinShift) >= tstar) {
+        kept |= 1u << r;
+        atomicAdd(&sub[sub_pad(sub_bucket(ge, hk[r]))], 1u);
+      }
     }
   }
   gsync(c);
   group_exclusive_scan_padded(c, sub, m_keep);  // sub(i) = first slot of sub-bucket i
   const uint32_t cap = top_k + kStageSlack;
 #pragma unroll
-  for (int r = 0; r < kPerThread; ++r) {
-    if ((kept >> r) & 1u) {
+  for (int r0 = 0; r0 < kPerThread; r0 += 8) {  // runs of 8 entries with no bit set are skipped
+    if (((kept >> r0) & 0xFFu) == 0u) continue;
+#pragma unroll
+    for (int r = r0; r < r0 + 8; ++r) {
+      if (!((kept >> r) & 1u)) continue;
       const uint32_t b = sub_bucket(ge, hk[r]);
       const uint32_t pos = atomicAdd(&sub[sub_pad(b)], 1u);
       if (pos < cap) {
