@@ -135,6 +135,28 @@ def test_monotone_and_tied_scores_on_a_split_tail(binding, dev, oracle_mod, dire
     parity.assert_exact(ids, sc, r_ids, r_sc)
 
 
+@pytest.mark.parametrize("kind", ["int", "normal"])
+def test_direct_store_boundary(binding, dev, oracle_mod, kind):
+    """Query blocks whose queries see at most 4096 keys append every visible key straight
+    to the store; one more visible key takes the filtered path. Segments with 4093-4096,
+    4094-4097 and 3-6 visible keys sit beside a 260-query segment (so nothing is split)."""
+    tq = [4, 4, 4, 260]
+    tk = [4096, 4097, 6, 300]
+    offs = [4092, 4093, 2, 40]
+    cu_q = np.concatenate([[0], np.cumsum(tq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(tk)]).astype(np.int32)
+    wl = inputs.draw(int(cu_q[-1]), int(cu_k[-1]), cu_q, cu_k, 2048, q_causal_offsets=offs, seed=31, kind=kind)
+    units = binding.indexer_topk_unit_table(binding.Desc(wl.T, wl.Tkv, cu_q, cu_k, 2048, offs))
+    assert len(units) == 3 + 65 and (units[:, 4] == 0).all()  # one unit per query block
+    ids, sc = run_plan(binding, wl, dev)
+    rows = np.arange(12)
+    if kind == "int":
+        r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl), rows=rows.astype(np.int32))
+        parity.assert_exact(ids, sc, r_ids, r_sc, rows=rows)
+    else:
+        parity.assert_close(ids, sc, wl, rows)
+
+
 def test_repeat_runs_bit_identical(binding, dev):
     wl = inputs.draw(200, 1500, [0, 200], [0, 1500], 256, seed=4, kind="normal")
     outs = run_plan(binding, wl, dev, runs=3)
