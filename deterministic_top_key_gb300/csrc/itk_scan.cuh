@@ -575,7 +575,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       // A unit whose queries see at most kCap keys of its tile range hands every visible
       // key over: the appends go straight to the store slots, with no histogram, no sync
       // points and no copy at the end (uniform across the CTA).
-      const bool direct = min(unit.w + unit.y, range.z * kBlockKeys) - range.y * kBlockKeys <= kCap;
+      const int visible = min(unit.w + unit.y, range.z * kBlockKeys) - range.y * kBlockKeys;  // most keys a query sees
+      const bool direct = visible <= kCap;
+      // Sync points raise the threshold and make room in the working buffer. A unit whose
+      // queries see at most kCompactAt keys can never fill its buffer, and its sync points
+      // cost more than the appends they save: it raises the threshold once, at the end.
+      const bool no_sync = visible <= static_cast<int>(kCompactAt);
       if (!direct)
         for (int i = c.gtid; i < kBins; i += 128) hist_g[i] = 0u;
       if (c.gtid < 4) qs[c.gtid] = 0u;
@@ -592,7 +597,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         float thr_f = -__int_as_float(0x7F800000);  // the lowest score of bin thr (bins below 4 hold no finite score)
         for (int tile = 0; tile < nt; ++tile, ++ac) {
           const int ab = ac & 1;
-          if (!kDirect && tile % kSyncEvery == sync_phase) {
+          if (!kDirect && !no_sync && tile % kSyncEvery == sync_phase) {
             // Group sync point (the only barriers inside a unit): every append of the
             // earlier tiles is done, so the count and the histogram are final.
             gsync(c);
