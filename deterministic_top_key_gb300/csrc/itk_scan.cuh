@@ -578,9 +578,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int visible = min(unit.w + unit.y, range.z * kBlockKeys) - range.y * kBlockKeys;  // most keys a query sees
       const bool direct = visible <= kCap;
       // Sync points raise the threshold and make room in the working buffer. A unit whose
-      // queries see at most kCompactAt keys can never fill its buffer, and its sync points
+      // queries see at most kQCap keys can never overflow its buffer, and its sync points
       // cost more than the appends they save: it raises the threshold once, at the end.
-      const bool no_sync = visible <= static_cast<int>(kCompactAt);
+      const bool no_sync = visible <= kQCap;
       if (!direct)
         for (int i = c.gtid; i < kBins; i += 128) hist_g[i] = 0u;
       if (c.gtid < 4) qs[c.gtid] = 0u;
