@@ -270,17 +270,28 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   gsync(c);
   if (flags[1] == 0u) {  // uniform: read by every thread before anyone writes it again
     const uint32_t staged = m_keep < cap ? m_keep : cap;
-    for (uint32_t j = c.gtid; j < staged; j += 128) {
-      const uint32_t b = bkt[j];
-      const uint32_t start = b ? sub[sub_pad(b - 1)] : 0u;
-      if (start >= keff) continue;
-      const uint32_t end = sub[sub_pad(b)];
-      const unsigned long long x = stage[j];
-      uint32_t pos = start;
-      for (uint32_t i = start; i < end; ++i) pos += stage[i] > x ? 1u : 0u;
-      if (pos < keff) {
-        st_stream_s32(out_ids + pos, static_cast<int32_t>(static_cast<uint32_t>(x & 0xFFFFFFFFull)));
-        st_stream_f32(out_scores + pos, key_to_float(static_cast<uint32_t>(x >> 32)));
+    constexpr int kSlots = 2;  // staged keys a thread places per pass (independent chains)
+    for (uint32_t j0 = c.gtid; j0 < staged; j0 += 128 * kSlots) {
+      uint32_t start[kSlots], end[kSlots];
+      unsigned long long x[kSlots];
+#pragma unroll
+      for (int u = 0; u < kSlots; ++u) {
+        const uint32_t j = j0 + 128u * u;
+        const bool v = j < staged;
+        const uint32_t b = v ? bkt[j] : 0u;
+        start[u] = v && b ? sub[sub_pad(b - 1)] : 0u;
+        end[u] = v ? sub[sub_pad(b)] : 0u;
+        if (start[u] >= keff) end[u] = start[u];  // lands at or past keff: nothing to place
+        x[u] = v ? stage[j] : 0ull;
+      }
+#pragma unroll
+      for (int u = 0; u < kSlots; ++u) {
+        uint32_t pos = start[u];
+        for (uint32_t i = start[u]; i < end[u]; ++i) pos += stage[i] > x[u] ? 1u : 0u;
+        if (end[u] > start[u] && pos < keff) {
+          st_stream_s32(out_ids + pos, static_cast<int32_t>(static_cast<uint32_t>(x[u] & 0xFFFFFFFFull)));
+          st_stream_f32(out_scores + pos, key_to_float(static_cast<uint32_t>(x[u] >> 32)));
+        }
       }
     }
     for (uint32_t r = keff + c.gtid; r < top_k; r += 128) {
