@@ -40,7 +40,11 @@
 // the score itself with the lowest score of the threshold bin, and forms the 64-bit key
 // only for the keys it appends. A unit whose queries see at most kCap keys of its tile
 // range skips the filter: every visible key goes straight to the store slot (no
-// histogram, no sync points, no hand-off copy); the tile loop is compiled for both cases.
+// histogram, no sync points, no hand-off copy). A unit whose queries see at most kQCap
+// keys has no sync points: every visible key goes to the working buffer and the
+// threshold is applied once, at the hand-off. In both, key j of the unit's tile range
+// has slot j (no slot reservation). The tile loop is compiled for the three kinds.
+// Scores are taken to be finite (inputs whose dot products overflow FP32 are out of scope).
 #pragma once
 
 #include <type_traits>
@@ -583,13 +587,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const bool no_sync = visible <= kQCap;
       if (!direct)
         for (int i = c.gtid; i < kBins; i += 128) hist_g[i] = 0u;
-      if (c.gtid < 4) qs[c.gtid] = 0u;
-      gsync(c);
       const int tile0 = range.y, nt = range.z - range.y;
       const int last_key = unit.w + g;  // causal bound: local keys 0..last_key are visible
-      // The tile loop, compiled once for direct units and once for the others.
-      auto scan_tiles = [&](auto direct_tag) -> bool {
-        constexpr bool kDirect = decltype(direct_tag)::value;
+      // units without sync points append every visible key, key j of the unit's range at
+      // slot j: the count is known from the start
+      const int mine = min(last_key + 1 - tile0 * kBlockKeys, nt * kBlockKeys);
+      if (c.gtid < 4) qs[c.gtid] = (c.gtid == 0 && no_sync && active) ? static_cast<uint32_t>(max(mine, 0)) : 0u;
+      gsync(c);
+      // The tile loop, compiled for three kinds of unit: direct (every visible key to the
+      // store), dense (every visible key to the working buffer, no sync points) and
+      // filtered (threshold raised at sync points).
+      auto scan_tiles = [&](auto mode_tag) -> bool {
+        constexpr int kMode = decltype(mode_tag)::value;
+        constexpr bool kDirect = kMode == 0;
+        constexpr bool kDense = kMode < 2;  // key j of the unit's tile range goes to slot j
         unsigned long long* app = kDirect ? p.store + (uidx * kQB + g) * kCap : cand;
         const uint64_t pol_app = kDirect ? pol_store : pol_cand;
         bool failed = false;
@@ -597,7 +608,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         float thr_f = -__int_as_float(0x7F800000);  // the lowest score of bin thr (bins below 4 hold no finite score)
         for (int tile = 0; tile < nt; ++tile, ++ac) {
           const int ab = ac & 1;
-          if (!kDirect && !no_sync && tile % kSyncEvery == sync_phase) {
+          if (!kDense && tile % kSyncEvery == sync_phase) {
             // Group sync point (the only barriers inside a unit): every append of the
             // earlier tiles is done, so the count and the histogram are final.
             gsync(c);
@@ -663,25 +674,36 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.ae(ab));
           }
-          // append the keys that pass the filter
-          const bool ins = active && jl <= last_key && score >= thr_f;  // == bin(score) >= thr for finite scores
-          const uint32_t m = __ballot_sync(0xFFFFFFFFu, ins);
-          if (m) {
-            const int lead = __ffs(m) - 1;
-            uint32_t base = 0u;
-            if (lane == lead) base = atomicAdd(&qs[0], static_cast<uint32_t>(__popc(m)));
-            base = __shfl_sync(0xFFFFFFFFu, base, lead);
-            if (ins) {
+          if constexpr (kDense) {  // every visible key, at the slot of its index (scores are finite)
+            if (active && jl <= last_key) {
               const uint32_t key32 = ord_key(score);
-              st_hint_u64(app + base + __popc(m & ((1u << lane) - 1u)),
+              st_hint_u64(app + tile * kBlockKeys + key_lane,
                           (static_cast<unsigned long long>(key32) << 32) | static_cast<uint32_t>(unit.z + jl), pol_app);
               if (!kDirect) hist_inc(hist_g, key32 >> kBinShift);
+            }
+          } else {
+            // append the keys that pass the filter
+            const bool ins = active && jl <= last_key && score >= thr_f;  // == bin(score) >= thr for finite scores
+            const uint32_t m = __ballot_sync(0xFFFFFFFFu, ins);
+            if (m) {
+              const int lead = __ffs(m) - 1;
+              uint32_t base = 0u;
+              if (lane == lead) base = atomicAdd(&qs[0], static_cast<uint32_t>(__popc(m)));
+              base = __shfl_sync(0xFFFFFFFFu, base, lead);
+              if (ins) {
+                const uint32_t key32 = ord_key(score);
+                st_hint_u64(app + base + __popc(m & ((1u << lane) - 1u)),
+                            (static_cast<unsigned long long>(key32) << 32) | static_cast<uint32_t>(unit.z + jl), pol_app);
+                if (!kDirect) hist_inc(hist_g, key32 >> kBinShift);
+              }
             }
           }
         }
         return failed;
       };
-      const bool failed = direct ? scan_tiles(std::true_type{}) : scan_tiles(std::false_type{});
+      const bool failed = direct    ? scan_tiles(std::integral_constant<int, 0>{})
+                          : no_sync ? scan_tiles(std::integral_constant<int, 1>{})
+                                    : scan_tiles(std::integral_constant<int, 2>{});
       if (failed) break;
       // Hand-off: every candidate of the unit's query goes to the store.
       gsync(c);  // every append of the unit is done
