@@ -91,15 +91,16 @@ __device__ __forceinline__ void ticket_release(TicketBlock* t) {
 
 // ------------------------------------------------------------------ 128-thread groups
 struct GroupCtx {
-  int gtid;        // 0..127
-  int gwarp;       // 0..3
+  int gtid;        // 0 .. nthr - 1
+  int gwarp;       // warp within the group
   int lane;
   uint32_t bar;    // named barrier id
+  uint32_t nthr = 128;  // threads in the group
   uint32_t* radix; // 256 words of radix-select scratch
   uint32_t* sel;   // 8 words of scratch
 };
 
-__device__ __forceinline__ void gsync(const GroupCtx& c) { named_bar_sync(c.bar, 128); }
+__device__ __forceinline__ void gsync(const GroupCtx& c) { named_bar_sync(c.bar, c.nthr); }
 
 // Warp-aggregated append: lanes with `pred` get consecutive slots from *counter.
 __device__ __forceinline__ uint32_t warp_append_slot(bool pred, uint32_t* counter, int lane) {

@@ -7,7 +7,7 @@
 // (the scan's filter only drops keys below top_k keys already seen), so selecting within
 // them gives the exact answer.
 //
-// Work distribution: a persistent grid; each 128-thread group draws one query at a time
+// Work distribution: a persistent grid; each 256-thread group draws one query at a time
 // from a self-resetting ticket word (same page, commit note on drawing work units from
 // the ticket word and the TicketWord note).
 //
@@ -27,21 +27,26 @@
 
 namespace itk {
 
-constexpr int kSelGroups = 4;                 // 128-thread groups per selection CTA
-constexpr int kSelThreads = kSelGroups * 128;
+constexpr int kSG = 256;                      // threads of a selection group (one query at a time)
+constexpr int kSelGroups = 4;                 // groups per selection CTA
+constexpr int kSelThreads = kSelGroups * kSG;
+constexpr int kSelWarps = kSG / 32;           // warps of a group
+constexpr int kSelPer = kCap / kSG;           // candidates a thread holds (entry gtid + kSG r)
+constexpr int kBinsPer = kBins / kSG;         // bins a thread scans in the suffix sums
+static_assert(kSelPer <= 32 && kSelPer % 8 == 0, "candidate masks are 32-bit, runs of 8");
 constexpr int kStageSlack = 256;              // staging slots past top_k
 constexpr int kBigBucket = 32;                // sub-buckets above this size take the full sort
 
 // Per-group shared memory of the selection kernel (offsets within the group's slice).
 // The bin and sub-bucket arrays carry one pad word per run of entries that one thread
-// scans (16 bins, 32 sub-buckets), so that the 32 lanes of a warp, each walking its own
-// run, hit 32 different banks.
-constexpr uint32_t kSgBins = 0;                                        // 2048 + 128 x u32
-constexpr uint32_t kSgSub = kSgBins + (kBins + kBins / 16) * 4;        // 4096 + 128 x u32
-constexpr uint32_t kSgStage = kSgSub + (kCap + kCap / 32) * 4;         // (2048 + 256) x u64
+// scans (kBinsPer bins, kSelPer sub-buckets), so that the 32 lanes of a warp, each
+// walking its own run, hit 32 different banks.
+constexpr uint32_t kSgBins = 0;                                        // 2048 + 256 x u32
+constexpr uint32_t kSgSub = kSgBins + (kBins + kBins / kBinsPer) * 4;  // 4096 + 256 x u32
+constexpr uint32_t kSgStage = kSgSub + (kCap + kCap / kSelPer) * 4;    // (2048 + 256) x u64
 constexpr uint32_t kSgRadix = kSgStage + (kMaxTopK + kStageSlack) * 8; // 256 x u32
-constexpr uint32_t kSgSel = kSgRadix + 256 * 4;                        // 8 x u32
-constexpr uint32_t kSgFlags = kSgSel + 8 * 4;                          // 4 x u32
+constexpr uint32_t kSgSel = kSgRadix + 256 * 4;                        // 16 x u32
+constexpr uint32_t kSgFlags = kSgSel + 16 * 4;                         // 4 x u32
 constexpr uint32_t kSgItem = kSgFlags + 4 * 4;                         // 4 x u32 (drawn item)
 constexpr uint32_t kSgBkt = kSgItem + 16;                              // (2048 + 256) x u16: sub-bucket of each staged key
 constexpr uint32_t kSgBytes = (kSgBkt + (kMaxTopK + kStageSlack) * 2 + 127) / 128 * 128;
@@ -49,8 +54,8 @@ constexpr uint32_t kSelSmemBytes = kSelGroups * kSgBytes;
 static_assert(kSgStage % 16 == 0, "alignment");
 static_assert(kSelSmemBytes <= 232448, "shared memory budget");
 
-__device__ __forceinline__ uint32_t bin_pad(uint32_t b) { return b + (b >> 4); }
-__device__ __forceinline__ uint32_t sub_pad(uint32_t i) { return i + (i >> 5); }
+__device__ __forceinline__ uint32_t bin_pad(uint32_t b) { return b + b / kBinsPer; }
+__device__ __forceinline__ uint32_t sub_pad(uint32_t i) { return i + i / kSelPer; }
 
 struct SelectParams {
   const int32_t* item_rows;           // per store slot: output row, or -1 (nothing to select there)
@@ -64,13 +69,13 @@ struct SelectParams {
   float* out_scores;                  // [T, top_k]
 };
 
-// Exclusive prefix sum of the padded array a (entry i at a[sub_pad(i)], i < n <= 128 *
-// kPerThread) in place, 128 threads, each scanning a run of kPerThread entries.
+// Exclusive prefix sum of the padded array a (entry i at a[sub_pad(i)], i < n <= kSG *
+// kSelPer) in place, kSG threads, each scanning a run of kSelPer entries.
 __device__ __forceinline__ void group_exclusive_scan_padded(const GroupCtx& c, uint32_t* a, uint32_t n) {
   uint32_t s = 0;
 #pragma unroll
-  for (int i = 0; i < kPerThread; ++i) {
-    const uint32_t idx = c.gtid * kPerThread + i;
+  for (int i = 0; i < kSelPer; ++i) {
+    const uint32_t idx = c.gtid * kSelPer + i;
     s += idx < n ? a[sub_pad(idx)] : 0u;
   }
   uint32_t incl = s;
@@ -83,10 +88,10 @@ __device__ __forceinline__ void group_exclusive_scan_padded(const GroupCtx& c, u
   gsync(c);
   uint32_t run = incl - s;
 #pragma unroll
-  for (int wv = 0; wv < 4; ++wv) run += wv < c.gwarp ? c.sel[4 + wv] : 0u;
+  for (int wv = 0; wv < kSelWarps; ++wv) run += wv < c.gwarp ? c.sel[4 + wv] : 0u;
 #pragma unroll
-  for (int i = 0; i < kPerThread; ++i) {  // second pass: the run is read again, not held
-    const uint32_t idx = c.gtid * kPerThread + i;
+  for (int i = 0; i < kSelPer; ++i) {  // second pass: the run is read again, not held
+    const uint32_t idx = c.gtid * kSelPer + i;
     if (idx < n) {
       const uint32_t x = a[sub_pad(idx)];
       a[sub_pad(idx)] = run;
@@ -100,7 +105,7 @@ __device__ __forceinline__ void group_exclusive_scan_padded(const GroupCtx& c, u
 __device__ void group_bitonic_desc(const GroupCtx& c, unsigned long long* a, uint32_t np2) {
   for (uint32_t size = 2; size <= np2; size <<= 1) {
     for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
-      for (uint32_t i = c.gtid; i < np2 / 2; i += 128) {
+      for (uint32_t i = c.gtid; i < np2 / 2; i += kSG) {
         const uint32_t lo = 2 * i - (i & (stride - 1));
         const uint32_t hi = lo + stride;
         const bool desc = (lo & size) == 0;
@@ -128,20 +133,54 @@ __device__ __forceinline__ uint32_t sub_bucket(const uint32_t* ge, uint32_t h) {
   return above + (cb - 1u - sub);
 }
 
+// Radix select over the group's register-held keys (entry r valid iff bit r of `valid`):
+// returns `prefix` with #{valid x : x >= prefix} == K (1 <= K <= valid keys; keys are
+// distinct). Digits of 8 bits from the top; stops as soon as the digit holding the K-th
+// largest key is selected whole.
+__device__ unsigned long long sel_group_select(const GroupCtx& c, const unsigned long long (&v)[kSelPer],
+                                               uint32_t valid, uint32_t K) {
+  unsigned long long prefix = 0ull;
+  uint32_t k_rem = K;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = c.gtid; i < 256; i += kSG) c.radix[i] = 0u;
+    gsync(c);
+    const unsigned long long hi_mask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
+#pragma unroll
+    for (int r = 0; r < kSelPer; ++r) {
+      if (((valid >> r) & 1u) && ((v[r] & hi_mask) == (prefix & hi_mask)))
+        atomicAdd(&c.radix[(v[r] >> shift) & 0xFFu], 1u);
+    }
+    gsync(c);
+    group_pick_digit(c, k_rem);
+    gsync(c);
+    const uint32_t b = c.sel[0];
+    k_rem = c.sel[1];
+    const uint32_t bucket = c.sel[2];
+    prefix |= static_cast<unsigned long long>(b) << shift;
+    if (bucket == k_rem) break;  // uniform across the group
+  }
+  gsync(c);  // c.sel may be reused right after
+  return prefix;
+}
+
 // Exact fallback for the one sub-bucket that crosses position keff and is too large to
 // sort in place (heavy ties): its `need` largest keys (bit r of in_b marks this thread's
-// members, entry gtid + 128 r of buf) go to stage[start ..), unsorted. Kept out of line so
+// members, entry gtid + kSG r of buf) go to stage[start ..), unsorted. Kept out of line so
 // that its 64-bit key registers do not weigh on the common path.
 __device__ __noinline__ void sel_crossing_fallback(const GroupCtx& c, const unsigned long long* buf, uint32_t n,
                                                    uint32_t in_b, uint32_t need, uint32_t start,
                                                    unsigned long long* stage, uint32_t* flags) {
-  unsigned long long v[kPerThread];
-  group_load(c, buf, n, v);
-  const unsigned long long pfx = group_select(c, v, in_b, need);
+  unsigned long long v[kSelPer];
+#pragma unroll
+  for (int r = 0; r < kSelPer; ++r) {
+    const uint32_t idx = c.gtid + static_cast<uint32_t>(kSG) * r;
+    v[r] = idx < n ? buf[idx] : 0ull;
+  }
+  const unsigned long long pfx = sel_group_select(c, v, in_b, need);
   if (c.gtid == 0) flags[3] = start;
   gsync(c);
 #pragma unroll
-  for (int r = 0; r < kPerThread; ++r) {
+  for (int r = 0; r < kSelPer; ++r) {
     const bool take = ((in_b >> r) & 1u) && v[r] >= pfx;
     const uint32_t slot = warp_append_slot(take, &flags[3], c.lane);
     if (take && slot < start + need) stage[slot] = v[r];  // exactly `need` keys qualify: keys are distinct
@@ -151,30 +190,30 @@ __device__ __noinline__ void sel_crossing_fallback(const GroupCtx& c, const unsi
 
 // Exact top-k of one query's n candidates (buf[0..n), n <= kCap), sorted by the total
 // order, written as one output row. Each thread holds the score keys (high words) of
-// candidates gtid + 128 r in registers; full 64-bit keys are read again from buf only to
+// candidates gtid + kSG r in registers; full 64-bit keys are read again from buf only to
 // place them.
 __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned long long* buf, uint32_t n,
                                            uint32_t top_k, uint32_t* ge, uint32_t* sub, unsigned long long* stage,
                                            uint16_t* bkt, uint32_t* flags, int32_t* out_ids, float* out_scores) {
   const uint32_t* buf_hi = reinterpret_cast<const uint32_t*>(buf) + 1;  // high word of entry i at buf_hi[2 i]
-  uint32_t hk[kPerThread];
-  // entry r of this thread is candidate gtid + 128 r: it exists for r < ceil((n - gtid) / 128)
-  const uint32_t n_mine = n > static_cast<uint32_t>(c.gtid) ? (n - c.gtid + 127u) / 128u : 0u;
+  uint32_t hk[kSelPer];
+  // entry r of this thread is candidate gtid + kSG r: it exists for r < ceil((n - gtid) / kSG)
+  const uint32_t n_mine = n > static_cast<uint32_t>(c.gtid) ? (n - c.gtid + kSG - 1u) / kSG : 0u;
   const uint32_t valid = n_mine >= 32u ? 0xFFFFFFFFu : (1u << n_mine) - 1u;
 #pragma unroll
-  for (int r = 0; r < kPerThread; ++r) hk[r] = 0u;
+  for (int r = 0; r < kSelPer; ++r) hk[r] = 0u;
 #pragma unroll
-  for (int r0 = 0; r0 < kPerThread; r0 += 8) {  // runs of 8 entries with no bit set are skipped
+  for (int r0 = 0; r0 < kSelPer; r0 += 8) {  // runs of 8 entries with no bit set are skipped
     if (((valid >> r0) & 0xFFu) == 0u) continue;
 #pragma unroll
     for (int r = r0; r < r0 + 8; ++r) {
       if (!((valid >> r) & 1u)) continue;
-      hk[r] = buf_hi[2 * (c.gtid + 128u * r)];
+      hk[r] = buf_hi[2 * (c.gtid + static_cast<uint32_t>(kSG) * r)];
     }
   }
   const uint32_t keff = n < top_k ? n : top_k;
   // count the candidates per bin
-  for (int i = c.gtid; i < kBins + kBins / 16; i += 128) ge[i] = 0u;
+  for (int i = c.gtid; i < kBins + kBins / kBinsPer; i += kSG) ge[i] = 0u;
   if (c.gtid == 0) {
     flags[0] = kBins - 1;    // first kept bin
     flags[1] = 0u;           // large sub-bucket seen
@@ -182,7 +221,7 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   }
   gsync(c);
 #pragma unroll
-  for (int r0 = 0; r0 < kPerThread; r0 += 8) {  // runs of 8 entries with no bit set are skipped
+  for (int r0 = 0; r0 < kSelPer; r0 += 8) {  // runs of 8 entries with no bit set are skipped
     if (((valid >> r0) & 0xFFu) == 0u) continue;
 #pragma unroll
     for (int r = r0; r < r0 + 8; ++r) {
@@ -191,13 +230,13 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
     }
   }
   gsync(c);
-  // ge(b) = candidates in bins >= b (suffix sums, 16 bins per thread, highest bins first)
+  // ge(b) = candidates in bins >= b (suffix sums, kBinsPer bins per thread, highest bins first)
   {
-    uint32_t loc[16];
+    uint32_t loc[kBinsPer];
     uint32_t s = 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      loc[i] = ge[bin_pad(kBins - 1 - (16 * c.gtid + i))];
+    for (int i = 0; i < kBinsPer; ++i) {
+      loc[i] = ge[bin_pad(kBins - 1 - (kBinsPer * c.gtid + i))];
       s += loc[i];
     }
     uint32_t incl = s;
@@ -210,11 +249,11 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
     gsync(c);
     uint32_t run = incl - s;
 #pragma unroll
-    for (int wv = 0; wv < 4; ++wv) run += wv < c.gwarp ? c.sel[4 + wv] : 0u;
+    for (int wv = 0; wv < kSelWarps; ++wv) run += wv < c.gwarp ? c.sel[4 + wv] : 0u;
     uint32_t first_kept = kBins - 1;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t b = kBins - 1 - (16 * c.gtid + i);
+    for (int i = 0; i < kBinsPer; ++i) {
+      const uint32_t b = kBins - 1 - (kBinsPer * c.gtid + i);
       // run = candidates in bins above b; bin b reaches a position below top_k iff run < top_k
       if (run < top_k) first_kept = b;
       run += loc[i];
@@ -225,11 +264,11 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   gsync(c);
   const uint32_t tstar = flags[0];
   const uint32_t m_keep = ge[bin_pad(tstar)];  // candidates in kept bins
-  for (uint32_t i = c.gtid; i < m_keep; i += 128) sub[sub_pad(i)] = 0u;
+  for (uint32_t i = c.gtid; i < m_keep; i += kSG) sub[sub_pad(i)] = 0u;
   gsync(c);
   uint32_t kept = 0;  // bit r: candidate r lies in a kept bin
 #pragma unroll
-  for (int r0 = 0; r0 < kPerThread; r0 += 8) {  // runs of 8 entries with no bit set are skipped
+  for (int r0 = 0; r0 < kSelPer; r0 += 8) {  // runs of 8 entries with no bit set are skipped
     if (((valid >> r0) & 0xFFu) == 0u) continue;
 #pragma unroll
     for (int r = r0; r < r0 + 8; ++r) {
@@ -244,7 +283,7 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   group_exclusive_scan_padded(c, sub, m_keep);  // sub(i) = first slot of sub-bucket i
   const uint32_t cap = top_k + kStageSlack;
 #pragma unroll
-  for (int r0 = 0; r0 < kPerThread; r0 += 8) {  // runs of 8 entries with no bit set are skipped
+  for (int r0 = 0; r0 < kSelPer; r0 += 8) {  // runs of 8 entries with no bit set are skipped
     if (((kept >> r0) & 0xFFu) == 0u) continue;
 #pragma unroll
     for (int r = r0; r < r0 + 8; ++r) {
@@ -252,7 +291,7 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
       const uint32_t b = sub_bucket(ge, hk[r]);
       const uint32_t pos = atomicAdd(&sub[sub_pad(b)], 1u);
       if (pos < cap) {
-        stage[pos] = buf[c.gtid + 128u * r];
+        stage[pos] = buf[c.gtid + static_cast<uint32_t>(kSG) * r];
         bkt[pos] = static_cast<uint16_t>(b);
       }
     }
@@ -261,7 +300,7 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   // sub(i) is now the end of sub-bucket i. Common case: every sub-bucket that reaches a
   // slot below keff is small and inside the staging area; each staged key's position is
   // then its sub-bucket's start plus the number of keys above it in that sub-bucket.
-  for (uint32_t i = c.gtid; i < m_keep; i += 128) {
+  for (uint32_t i = c.gtid; i < m_keep; i += kSG) {
     const uint32_t start = i ? sub[sub_pad(i - 1)] : 0u;
     const uint32_t end = sub[sub_pad(i)];
     if (start >= keff || end - start < 2) continue;
@@ -271,12 +310,12 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   if (flags[1] == 0u) {  // uniform: read by every thread before anyone writes it again
     const uint32_t staged = m_keep < cap ? m_keep : cap;
     constexpr int kSlots = 2;  // staged keys a thread places per pass (independent chains)
-    for (uint32_t j0 = c.gtid; j0 < staged; j0 += 128 * kSlots) {
+    for (uint32_t j0 = c.gtid; j0 < staged; j0 += kSG * kSlots) {
       uint32_t start[kSlots], end[kSlots];
       unsigned long long x[kSlots];
 #pragma unroll
       for (int u = 0; u < kSlots; ++u) {
-        const uint32_t j = j0 + 128u * u;
+        const uint32_t j = j0 + static_cast<uint32_t>(kSG) * u;
         const bool v = j < staged;
         const uint32_t b = v ? bkt[j] : 0u;
         start[u] = v && b ? sub[sub_pad(b - 1)] : 0u;
@@ -294,7 +333,7 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
         }
       }
     }
-    for (uint32_t r = keff + c.gtid; r < top_k; r += 128) {
+    for (uint32_t r = keff + c.gtid; r < top_k; r += kSG) {
       st_stream_s32(out_ids + r, -1);
       st_stream_f32(out_scores + r, -__int_as_float(0x7F800000));
     }
@@ -306,7 +345,7 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   gsync(c);
   // Heavy ties: sort every sub-bucket that reaches a slot below top_k in place, resolve
   // an oversized crossing sub-bucket exactly, and sort the whole range when needed.
-  for (uint32_t i = c.gtid; i < m_keep; i += 128) {
+  for (uint32_t i = c.gtid; i < m_keep; i += kSG) {
     const uint32_t start = i ? sub[sub_pad(i - 1)] : 0u;
     const uint32_t end = sub[sub_pad(i)];
     if (start >= keff || end - start < 2) continue;
@@ -334,7 +373,7 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
     const uint32_t start = over ? sub[sub_pad(over - 1)] : 0u;
     uint32_t in_b = 0;
 #pragma unroll
-    for (int r = 0; r < kPerThread; ++r)
+    for (int r = 0; r < kSelPer; ++r)
       if (((kept >> r) & 1u) && sub_bucket(ge, hk[r]) == over) in_b |= 1u << r;
     sel_crossing_fallback(c, buf, n, in_b, keff - start, start, stage, flags);
     if (c.gtid == 0) flags[1] = 1u;  // the refilled range is unsorted
@@ -343,11 +382,11 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   if (flags[1]) {
     uint32_t np2 = 2;
     while (np2 < keff) np2 <<= 1;
-    for (uint32_t i = keff + c.gtid; i < np2; i += 128) stage[i] = 0ull;
+    for (uint32_t i = keff + c.gtid; i < np2; i += kSG) stage[i] = 0ull;
     gsync(c);
     group_bitonic_desc(c, stage, np2);
   }
-  for (uint32_t r = c.gtid; r < top_k; r += 128) {
+  for (uint32_t r = c.gtid; r < top_k; r += kSG) {
     if (r < keff) {
       const unsigned long long x = stage[r];
       st_stream_s32(out_ids + r, static_cast<int32_t>(static_cast<uint32_t>(x & 0xFFFFFFFFull)));
@@ -363,11 +402,12 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
 __global__ void __launch_bounds__(kSelThreads, 1) indexer_topk_select_kernel(const SelectParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  const int g = threadIdx.x >> 7;
+  const int g = threadIdx.x / kSG;
   uint8_t* gs = smem + g * kSgBytes;
   GroupCtx c;
-  c.gtid = threadIdx.x & 127;
+  c.gtid = threadIdx.x % kSG;
   c.gwarp = c.gtid >> 5;
+  c.nthr = kSG;
   c.lane = threadIdx.x & 31;
   c.bar = 1 + g;
   c.radix = reinterpret_cast<uint32_t*>(gs + kSgRadix);
