@@ -43,7 +43,9 @@
 // histogram, no sync points, no hand-off copy). A unit whose queries see at most kQCap
 // keys has no sync points: every visible key goes to the working buffer and the
 // threshold is applied once, at the hand-off. In both, key j of the unit's tile range
-// has slot j (no slot reservation). The tile loop is compiled for the three kinds.
+// has slot j (no slot reservation). A longer unit does the same over its first kQCap
+// keys, then raises the threshold, compacts, and filters from there on with sync
+// points. The tile loop is compiled for the three kinds.
 // Scores are taken to be finite (inputs whose dot products overflow FP32 are out of scope).
 #pragma once
 
@@ -56,6 +58,7 @@ namespace itk {
 constexpr int kN = kQB * kHeads;             // MMA N = 256 (query, head) columns
 constexpr int kStages = 3;                   // K tile ring depth
 constexpr int kQCap = 16384;                 // working buffer entries per query while a unit runs
+constexpr int kDenseTiles = kQCap / 128;     // tiles a filtered unit appends densely before its first sync
 constexpr int kSyncEvery = 32;               // epilogue group synchronizes every this many tiles
 constexpr uint32_t kCompactAt = kQCap - kSyncEvery * kBlockKeys;  // buffer fill that triggers a compaction
 constexpr int kEpiGroups = kQB;              // one 4-warp epilogue group per query of the unit
@@ -592,7 +595,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       // units without sync points append every visible key, key j of the unit's range at
       // slot j: the count is known from the start
       const int mine = min(last_key + 1 - tile0 * kBlockKeys, nt * kBlockKeys);
-      if (c.gtid < 4) qs[c.gtid] = (c.gtid == 0 && no_sync && active) ? static_cast<uint32_t>(max(mine, 0)) : 0u;
+      // (a filtered unit's first kDenseTiles tiles are appended the same way, so at most
+      // kQCap keys before its first sync point)
+      if (c.gtid < 4) qs[c.gtid] = (c.gtid == 0 && active) ? static_cast<uint32_t>(min(max(mine, 0), kQCap)) : 0u;
       gsync(c);
       // The tile loop, compiled for three kinds of unit: direct (every visible key to the
       // store), dense (every visible key to the working buffer, no sync points) and
@@ -608,7 +613,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         float thr_f = -__int_as_float(0x7F800000);  // the lowest score of bin thr (bins below 4 hold no finite score)
         for (int tile = 0; tile < nt; ++tile, ++ac) {
           const int ab = ac & 1;
-          if (!kDense && tile % kSyncEvery == sync_phase) {
+          // A filtered unit appends its first kDenseTiles tiles densely (slot = key index,
+          // no sync points), then raises the threshold and compacts once, then filters.
+          if (!kDense && (tile == kDenseTiles || (tile > kDenseTiles && tile % kSyncEvery == sync_phase))) {
             // Group sync point (the only barriers inside a unit): every append of the
             // earlier tiles is done, so the count and the histogram are final.
             gsync(c);
@@ -674,7 +681,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.ae(ab));
           }
-          if constexpr (kDense) {  // every visible key, at the slot of its index (scores are finite)
+          if (kDense || tile < kDenseTiles) {  // every visible key, at the slot of its index (scores are finite)
             if (active && jl <= last_key) {
               const uint32_t key32 = ord_key(score);
               st_hint_u64(app + tile * kBlockKeys + key_lane,
