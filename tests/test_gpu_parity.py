@@ -157,6 +157,30 @@ def test_direct_store_boundary(binding, dev, oracle_mod, kind):
         parity.assert_close(ids, sc, wl, rows)
 
 
+@pytest.mark.parametrize("kind", ["int", "normal"])
+def test_filtered_unit_boundary(binding, dev, oracle_mod, kind):
+    """A query block whose last query sees 16385 keys is filtered: its first 128 tiles go
+    to positional slots, then it compacts and filters. Its first three queries see
+    16382-16384 keys, so their positional prefix ends early. Beside it: a block whose
+    queries see 16381-16384 keys (no sync points at all), and a 260-query segment so that
+    nothing is split."""
+    tq = [4, 4, 260]
+    tk = [16385, 16384, 300]
+    offs = [16381, 16380, 40]
+    cu_q = np.concatenate([[0], np.cumsum(tq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(tk)]).astype(np.int32)
+    wl = inputs.draw(int(cu_q[-1]), int(cu_k[-1]), cu_q, cu_k, 2048, q_causal_offsets=offs, seed=37, kind=kind)
+    units = binding.indexer_topk_unit_table(binding.Desc(wl.T, wl.Tkv, cu_q, cu_k, 2048, offs))
+    assert len(units) == 2 + 65 and (units[:, 4] == 0).all()  # one unit per query block
+    ids, sc = run_plan(binding, wl, dev)
+    rows = np.arange(8)
+    if kind == "int":
+        r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl), rows=rows.astype(np.int32))
+        parity.assert_exact(ids, sc, r_ids, r_sc, rows=rows)
+    else:
+        parity.assert_close(ids, sc, wl, rows)
+
+
 def test_repeat_runs_bit_identical(binding, dev):
     wl = inputs.draw(200, 1500, [0, 200], [0, 1500], 256, seed=4, kind="normal")
     outs = run_plan(binding, wl, dev, runs=3)
