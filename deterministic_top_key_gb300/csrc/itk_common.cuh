@@ -1,6 +1,6 @@
-// Definitions shared by the scan kernel and the selection kernel: problem constants, the
-// 64-bit selection key, the work-unit and ticket records, and the 128-thread group
-// primitives (prefix sums, radix select, aggregated appends).
+// Definitions shared by the scan, merge and selection kernels: problem constants, the
+// 64-bit selection key, the work-unit and ticket records, and the thread-group primitives
+// (named-barrier sync, radix digit pick, aggregated appends).
 //
 // Operation: flashinfer PR #8691 ("perf(cake_dsa_indexer_det): ticket scheduling on
 // sm_107a, no fill kernel in eager entry"), opening description -- BF16 q/k, FP32 w and
@@ -27,7 +27,6 @@ constexpr int kQB = 4;                       // queries per work unit
 constexpr int kBlockKeys = 128;              // keys per tile (MMA M)
 constexpr int kMaxTopK = 2048;
 constexpr int kCap = 4096;                   // candidates per query handed from the scan to the selection
-constexpr int kPerThread = kCap / 128;       // candidates a 128-thread group holds per thread
 constexpr int kBinShift = 21;                // histogram bin = top 11 bits of the 32-bit score key
 constexpr int kBins = 1 << (32 - kBinShift); // 2048 bins
 constexpr int kMaxMergeChunks = 256;         // chunks (units) a split query's keys may span
@@ -145,49 +144,6 @@ __device__ __forceinline__ void group_pick_digit(const GroupCtx& c, uint32_t k_r
       above += cnt[i];
     }
   }
-}
-
-// Radix select over keys held in registers (entry r valid iff bit r of `valid`): returns
-// `prefix` with #{valid x : x >= prefix} == K (1 <= K <= number of valid keys; keys are
-// distinct). Digits of 8 bits from the top; stops as soon as the digit holding the K-th
-// largest key is selected whole.
-__device__ unsigned long long group_select(const GroupCtx& c, const unsigned long long (&v)[kPerThread],
-                                           uint32_t valid, uint32_t K) {
-  unsigned long long prefix = 0ull;
-  uint32_t k_rem = K;
-  for (int shift = 56; shift >= 0; shift -= 8) {
-    for (int i = c.gtid; i < 256; i += 128) c.radix[i] = 0u;
-    gsync(c);
-    const unsigned long long hi_mask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
-#pragma unroll
-    for (int r = 0; r < kPerThread; ++r) {
-      if (((valid >> r) & 1u) && ((v[r] & hi_mask) == (prefix & hi_mask)))
-        atomicAdd(&c.radix[(v[r] >> shift) & 0xFFu], 1u);
-    }
-    gsync(c);
-    group_pick_digit(c, k_rem);
-    gsync(c);
-    const uint32_t b = c.sel[0];
-    k_rem = c.sel[1];
-    const uint32_t bucket = c.sel[2];
-    prefix |= static_cast<unsigned long long>(b) << shift;
-    if (bucket == k_rem) break;  // uniform across the group
-  }
-  gsync(c);  // c.sel may be reused right after
-  return prefix;
-}
-
-// Loads the first n keys of buf into registers (entry gtid + 128*r); returns the valid mask.
-__device__ __forceinline__ uint32_t group_load(const GroupCtx& c, const unsigned long long* buf, uint32_t n,
-                                               unsigned long long (&v)[kPerThread]) {
-  uint32_t valid = 0;
-#pragma unroll
-  for (int r = 0; r < kPerThread; ++r) {
-    const uint32_t idx = c.gtid + 128u * r;
-    v[r] = idx < n ? buf[idx] : 0ull;
-    valid |= (idx < n ? 1u : 0u) << r;
-  }
-  return valid;
 }
 
 }  // namespace itk
