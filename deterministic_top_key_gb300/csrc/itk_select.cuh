@@ -47,7 +47,7 @@ constexpr uint32_t kSgStage = kSgSub + (kCap + kCap / kSelPer) * 4;    // (2048 
 constexpr uint32_t kSgRadix = kSgStage + (kMaxTopK + kStageSlack) * 8; // 256 x u32
 constexpr uint32_t kSgSel = kSgRadix + 256 * 4;                        // 16 x u32
 constexpr uint32_t kSgFlags = kSgSel + 16 * 4;                         // 4 x u32
-constexpr uint32_t kSgItem = kSgFlags + 4 * 4;                         // 4 x u32 (drawn item)
+constexpr uint32_t kSgItem = kSgFlags + 4 * 4;                         // drawn item (u64), its row and count
 constexpr uint32_t kSgBkt = kSgItem + 16;                              // (2048 + 256) x u16: sub-bucket of each staged key
 constexpr uint32_t kSgBytes = (kSgBkt + (kMaxTopK + kStageSlack) * 2 + 127) / 128 * 128;
 constexpr uint32_t kSelSmemBytes = kSelGroups * kSgBytes;
@@ -421,22 +421,44 @@ __global__ void __launch_bounds__(kSelThreads, 1) indexer_topk_select_kernel(con
   const unsigned long long n_items = static_cast<unsigned long long>(p.n_items);
   grid_dep_wait();  // the scan (and merge) that wrote the candidates is complete
 
-  while (true) {
-    if (c.gtid == 0) *s_item = atomicAdd(&p.ticket->next, 1ull);
-    gsync(c);
-    const unsigned long long item = *s_item;
-    gsync(c);  // every thread has read the item before the next draw overwrites it
-    if (item >= n_items) break;
-    const int32_t out_row = p.item_rows[item];
-    if (out_row < 0) continue;
-    const size_t row = static_cast<size_t>(out_row);
-    uint32_t n = p.counts[item];
-    if (n > static_cast<uint32_t>(kCap)) {  // cannot happen: the scan hands off at most kCap keys
-      if (c.gtid == 0) atomicOr(p.status, kStatusInternal | (20u << 8));
-      n = kCap;
+  // Items are drawn one ahead: thread 0 draws the next item (and reads its output row and
+  // candidate count) while the group works on the current one, hiding those latencies.
+  volatile uint32_t* s_meta = reinterpret_cast<volatile uint32_t*>(gs + kSgItem + 8);  // [0] row, [1] count
+  auto publish = [&](unsigned long long it) {  // thread 0 only
+    int32_t r = -1;
+    uint32_t cnt = 0;
+    if (it < n_items) {
+      r = p.item_rows[it];
+      cnt = p.counts[it];
     }
-    sel_finish(c, p.store + item * kCap, n, static_cast<uint32_t>(p.top_k), ge, sub, stage, bkt, flags,
-               p.out_ids + row * p.top_k, p.out_scores + row * p.top_k);
+    *s_item = it;
+    s_meta[0] = static_cast<uint32_t>(r);
+    s_meta[1] = cnt;
+  };
+  if (c.gtid == 0) publish(atomicAdd(&p.ticket->next, 1ull));
+  gsync(c);
+  unsigned long long item = *s_item;
+  int32_t out_row = static_cast<int32_t>(s_meta[0]);
+  uint32_t n = s_meta[1];
+  gsync(c);  // every thread has read the item before the next one is published
+  while (item < n_items) {
+    unsigned long long next = 0ull;
+    if (c.gtid == 0) next = atomicAdd(&p.ticket->next, 1ull);  // used after this item's work
+    if (out_row >= 0) {
+      if (n > static_cast<uint32_t>(kCap)) {  // cannot happen: the scan hands off at most kCap keys
+        if (c.gtid == 0) atomicOr(p.status, kStatusInternal | (20u << 8));
+        n = kCap;
+      }
+      const size_t row = static_cast<size_t>(out_row);
+      sel_finish(c, p.store + item * kCap, n, static_cast<uint32_t>(p.top_k), ge, sub, stage, bkt, flags,
+                 p.out_ids + row * p.top_k, p.out_scores + row * p.top_k);
+    }
+    if (c.gtid == 0) publish(next);
+    gsync(c);
+    item = *s_item;
+    out_row = static_cast<int32_t>(s_meta[0]);
+    n = s_meta[1];
+    gsync(c);  // every thread has read the item before the next one is published
   }
   __syncthreads();
   if (threadIdx.x == 0) ticket_release(p.ticket);
