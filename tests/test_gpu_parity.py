@@ -181,6 +181,27 @@ def test_filtered_unit_boundary(binding, dev, oracle_mod, kind):
         parity.assert_close(ids, sc, wl, rows)
 
 
+@pytest.mark.parametrize("top_k", [1, 7, 300])
+@pytest.mark.parametrize("kind", ["int", "normal"])
+def test_small_top_k_in_every_append_mode(binding, dev, oracle_mod, top_k, kind):
+    """Small top_k through the three append modes of the scan: query blocks that see at
+    most 4096 keys (straight to the store), at most 16384 (positional, no sync points)
+    and 20000 (positional prefix, then filtered with sync points and compactions)."""
+    tq = [4, 4, 4, 260]
+    tk = [3000, 10000, 20000, 300]
+    cu_q = np.concatenate([[0], np.cumsum(tq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(tk)]).astype(np.int32)
+    wl = inputs.draw(int(cu_q[-1]), int(cu_k[-1]), cu_q, cu_k, top_k, seed=41, kind=kind)
+    assert len(binding.indexer_topk_unit_table(binding.Desc(wl.T, wl.Tkv, cu_q, cu_k, top_k))) == 3 + 65
+    ids, sc = run_plan(binding, wl, dev)
+    rows = np.arange(12)
+    if kind == "int":
+        r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl), rows=rows.astype(np.int32))
+        parity.assert_exact(ids, sc, r_ids, r_sc, rows=rows)
+    else:
+        parity.assert_close(ids, sc, wl, rows)
+
+
 def test_repeat_runs_bit_identical(binding, dev):
     wl = inputs.draw(200, 1500, [0, 200], [0, 1500], 256, seed=4, kind="normal")
     outs = run_plan(binding, wl, dev, runs=3)
