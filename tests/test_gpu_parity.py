@@ -260,6 +260,21 @@ def test_split_tail_matches_unsplit(binding, dev, oracle_mod, kind):
         parity.assert_close(ids_s, sc_s, small, np.arange(4))
 
 
+@pytest.mark.parametrize("kind", ["int", "normal"])
+def test_split_tail_with_fewer_keys_than_top_k(binding, dev, oracle_mod, kind):
+    """Four queries over 1500 keys, top_k 2048: the split tail's merge keeps every key and
+    fills the rest of each row."""
+    wl = inputs.draw(4, 1500, [0, 4], [0, 1500], 2048, seed=43, kind=kind)
+    assert len(binding.indexer_topk_unit_table(binding.Desc(4, 1500, [0, 4], [0, 1500], 2048))) > 1
+    ids, sc = run_plan(binding, wl, dev)
+    if kind == "int":
+        r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl))
+        parity.assert_exact(ids, sc, r_ids, r_sc)
+    else:
+        parity.assert_close(ids, sc, wl, np.arange(4))
+    assert (ids[:, 1500:] == -1).all()
+
+
 def test_eager_matches_prepared_on_a_split_tail(binding, dev):
     """The eager entry runs the same launches (the scan, then the merge) for a split tail."""
     import torch
