@@ -28,9 +28,9 @@
  *
  * Prepared-runner contract (same page, commit note "TicketWord ... ABI dsa_indexer_v4" and
  * the review comment on stream ordering of prepared runners): prepare once per shape / segment layout / top_k, then run many
- * times with any buffers. The plan owns a 16-byte ticket block, zeroed once at prepare
- * on the prepare stream; every completed scan leaves it at zero again, so a run issues
- * no memset. Prepare and run on the same stream, or order the two streams yourself:
+ * times with any buffers. The plan owns its 16-byte ticket blocks (one for the scan, one
+ * for the selection), zeroed once at prepare on the prepare stream; every completed run
+ * leaves them at zero again, so a run issues no memset. Prepare and run on the same stream, or order the two streams yourself:
  * the zeroing is queued on the prepare stream and nothing orders it before a run on
  * another stream. After a run whose launch failed, the next run zeroes the block on its
  * stream before the scan.
@@ -40,7 +40,10 @@
  * failure on the calling thread.
  *
  * Streams are passed as void* and must be a cudaStream_t (NULL = legacy default stream).
- * All device pointers are device (or managed) memory of the current CUDA device.
+ * All device pointers are device (or managed) memory of the current CUDA device. A run's
+ * kernels are launched as programmatic dependents of the kernel before them on the
+ * stream: their CTAs may start while that kernel finishes, and wait for it to complete
+ * (griddepcontrol.wait) before they read any of its results, so stream order holds.
  */
 #ifndef DTK_INDEXER_TOPK_H_
 #define DTK_INDEXER_TOPK_H_
