@@ -299,15 +299,11 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   gsync(c);
   // sub(i) is now the end of sub-bucket i. Common case: every sub-bucket that reaches a
   // slot below keff is small and inside the staging area; each staged key's position is
-  // then its sub-bucket's start plus the number of keys above it in that sub-bucket.
-  for (uint32_t i = c.gtid; i < m_keep; i += kSG) {
-    const uint32_t start = i ? sub[sub_pad(i - 1)] : 0u;
-    const uint32_t end = sub[sub_pad(i)];
-    if (start >= keff || end - start < 2) continue;
-    if (end - start > static_cast<uint32_t>(kBigBucket) || (end > keff && end > cap)) flags[1] = 1u;
-  }
-  gsync(c);
-  if (flags[1] == 0u) {  // uniform: read by every thread before anyone writes it again
+  // then its sub-bucket's start plus the number of keys above it in that sub-bucket. A
+  // thread that meets a large sub-bucket (or one that runs past the staging area) skips
+  // it and raises flags[1]; the exact path below then rewrites the whole row.
+  {  // optimistic placement: a heavy sub-bucket sets flags[1], and the exact path below rewrites the row
+    bool heavy = false;
     const uint32_t staged = m_keep < cap ? m_keep : cap;
     constexpr int kSlots = 2;  // staged keys a thread places per pass (independent chains)
     for (uint32_t j0 = c.gtid; j0 < staged; j0 += kSG * kSlots) {
@@ -322,6 +318,10 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
         end[u] = v ? sub[sub_pad(b)] : 0u;
         if (start[u] >= keff) end[u] = start[u];  // lands at or past keff: nothing to place
         x[u] = v ? stage[j] : 0ull;
+        if (end[u] - start[u] > static_cast<uint32_t>(kBigBucket) || (end[u] > keff && end[u] > cap)) {
+          heavy = true;
+          end[u] = start[u];
+        }
       }
 #pragma unroll
       for (int u = 0; u < kSlots; ++u) {
@@ -337,6 +337,10 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
       st_stream_s32(out_ids + r, -1);
       st_stream_f32(out_scores + r, -__int_as_float(0x7F800000));
     }
+    if (heavy) flags[1] = 1u;
+  }
+  gsync(c);
+  if (flags[1] == 0u) {  // uniform: read by every thread before anyone writes it again
     gsync(c);
     return;
   }
