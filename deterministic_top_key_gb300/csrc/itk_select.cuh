@@ -28,7 +28,7 @@
 namespace itk {
 
 constexpr int kSG = 256;                      // threads of a selection group (one query at a time)
-constexpr int kSelGroups = 4;                 // groups per selection CTA
+constexpr int kSelGroups = 3;                 // groups per selection CTA (80 registers a thread)
 constexpr int kSelThreads = kSelGroups * kSG;
 constexpr int kSelWarps = kSG / 32;           // warps of a group
 constexpr int kSelPer = kCap / kSG;           // candidates a thread holds (entry gtid + kSG r)
@@ -189,26 +189,24 @@ __device__ __noinline__ void sel_crossing_fallback(const GroupCtx& c, const unsi
 }
 
 // Exact top-k of one query's n candidates (buf[0..n), n <= kCap), sorted by the total
-// order, written as one output row. Each thread holds the score keys (high words) of
-// candidates gtid + kSG r in registers; full 64-bit keys are read again from buf only to
-// place them.
+// order, written as one output row. Each thread holds the 64-bit keys of candidates
+// gtid + kSG r in registers.
 __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned long long* buf, uint32_t n,
                                            uint32_t top_k, uint32_t* ge, uint32_t* sub, unsigned long long* stage,
                                            uint16_t* bkt, uint32_t* flags, int32_t* out_ids, float* out_scores) {
-  const uint32_t* buf_hi = reinterpret_cast<const uint32_t*>(buf) + 1;  // high word of entry i at buf_hi[2 i]
-  uint32_t hk[kSelPer];
+  unsigned long long vk[kSelPer];  // full 64-bit keys; the score word is the high half
   // entry r of this thread is candidate gtid + kSG r: it exists for r < ceil((n - gtid) / kSG)
   const uint32_t n_mine = n > static_cast<uint32_t>(c.gtid) ? (n - c.gtid + kSG - 1u) / kSG : 0u;
   const uint32_t valid = n_mine >= 32u ? 0xFFFFFFFFu : (1u << n_mine) - 1u;
 #pragma unroll
-  for (int r = 0; r < kSelPer; ++r) hk[r] = 0u;
+  for (int r = 0; r < kSelPer; ++r) vk[r] = 0ull;
 #pragma unroll
   for (int r0 = 0; r0 < kSelPer; r0 += 8) {  // runs of 8 entries with no bit set are skipped
     if (((valid >> r0) & 0xFFu) == 0u) continue;
 #pragma unroll
     for (int r = r0; r < r0 + 8; ++r) {
       if (!((valid >> r) & 1u)) continue;
-      hk[r] = buf_hi[2 * (c.gtid + static_cast<uint32_t>(kSG) * r)];
+      vk[r] = buf[c.gtid + static_cast<uint32_t>(kSG) * r];
     }
   }
   const uint32_t keff = n < top_k ? n : top_k;
@@ -226,7 +224,7 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
 #pragma unroll
     for (int r = r0; r < r0 + 8; ++r) {
       if (!((valid >> r) & 1u)) continue;
-      atomicAdd(&ge[bin_pad(hk[r] >> kBinShift)], 1u);
+      atomicAdd(&ge[bin_pad(static_cast<uint32_t>(vk[r] >> 32) >> kBinShift)], 1u);
     }
   }
   gsync(c);
@@ -273,9 +271,9 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
 #pragma unroll
     for (int r = r0; r < r0 + 8; ++r) {
       if (!((valid >> r) & 1u)) continue;
-      if ((hk[r] >> kBinShift) >= tstar) {
+      if ((static_cast<uint32_t>(vk[r] >> 32) >> kBinShift) >= tstar) {
         kept |= 1u << r;
-        atomicAdd(&sub[sub_pad(sub_bucket(ge, hk[r]))], 1u);
+        atomicAdd(&sub[sub_pad(sub_bucket(ge, static_cast<uint32_t>(vk[r] >> 32)))], 1u);
       }
     }
   }
@@ -288,10 +286,10 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
 #pragma unroll
     for (int r = r0; r < r0 + 8; ++r) {
       if (!((kept >> r) & 1u)) continue;
-      const uint32_t b = sub_bucket(ge, hk[r]);
+      const uint32_t b = sub_bucket(ge, static_cast<uint32_t>(vk[r] >> 32));
       const uint32_t pos = atomicAdd(&sub[sub_pad(b)], 1u);
       if (pos < cap) {
-        stage[pos] = buf[c.gtid + static_cast<uint32_t>(kSG) * r];
+        stage[pos] = vk[r];
         bkt[pos] = static_cast<uint16_t>(b);
       }
     }
@@ -378,7 +376,7 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
     uint32_t in_b = 0;
 #pragma unroll
     for (int r = 0; r < kSelPer; ++r)
-      if (((kept >> r) & 1u) && sub_bucket(ge, hk[r]) == over) in_b |= 1u << r;
+      if (((kept >> r) & 1u) && sub_bucket(ge, static_cast<uint32_t>(vk[r] >> 32)) == over) in_b |= 1u << r;
     sel_crossing_fallback(c, buf, n, in_b, keff - start, start, stage, flags);
     if (c.gtid == 0) flags[1] = 1u;  // the refilled range is unsorted
     gsync(c);
