@@ -20,6 +20,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -102,7 +103,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples: $ITK_CLOCKS_DIR if set, else the temporary directory
+        out_dir = os.environ.get("ITK_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"itk_clocks_rank{gpu_index}.csv")
         self.timed = None  # (t0, t1) host wall clock of the timed region
 
     def __enter__(self):

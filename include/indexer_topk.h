@@ -195,7 +195,8 @@ ITK_API const char* indexer_topk_version(void);
  * candidate store, work-unit table, ticket blocks, status word) lives in one static
  * device array of indexer_topk_noalloc_scratch_bytes() bytes (about 159 MB) that every
  * GPU loading this library holds until the process exits. The store holds 512 work units
- * (2048 queries); larger inputs run as one scan + selection launch pair per 512 units. The paper has no counterpart: it exists for
+ * (2048 queries); larger inputs run as one scan + selection launch pair per 512 units. The
+ * flashinfer PR page has no counterpart of this entry point: it exists for
  * callers that must not call cudaMalloc at call time -- a serving runtime or framework
  * that has already reserved the device memory for its own pool, or a latency-critical
  * path where an allocation, which can synchronize the device, is not acceptable.
