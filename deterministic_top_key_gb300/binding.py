@@ -115,7 +115,7 @@ class Desc:
         self.offs = None if q_causal_offsets is None else np.ascontiguousarray(q_causal_offsets, dtype=np.int32)
         self.c = _Desc(int(T), int(Tkv), int(H), int(D), int(top_k), len(self.cu_q) - 1, self.cu_q.ctypes.data,
                        self.cu_k.ctypes.data, None if self.offs is None else self.offs.ctypes.data)
-        self.T, self.Tkv, self.top_k = int(T), int(Tkv), int(top_k)
+        self.T, self.Tkv, self.top_k, self.H, self.D = int(T), int(Tkv), int(top_k), int(H), int(D)
 
     def ref(self):
         return ctypes.byref(self.c)
@@ -131,6 +131,37 @@ def _stream_handle(stream):
 
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _check_buffers(desc: Desc, q, k, w, out_ids, out_scores, workspace=None):
+    """The checks the C ABI cannot make on plain pointers: every tensor given is a
+    contiguous CUDA tensor of the expected dtype, on q's device, holding at least the
+    elements the call reads or writes (a flat buffer is fine: the library reads rows of
+    H*D, D and H elements and writes rows of top_k). A missing buffer (None) is left to the
+    library, which reports ITK_ERR_NULL_POINTER; alignment is checked there too."""
+    import torch
+
+    T, Tkv, K, H, D = desc.T, desc.Tkv, desc.top_k, desc.H, desc.D
+    want = (("q", q, torch.bfloat16, T * H * D), ("k", k, torch.bfloat16, Tkv * D), ("w", w, torch.float32, T * H),
+            ("out_ids", out_ids, torch.int32, T * K), ("out_scores", out_scores, torch.float32, T * K),
+            ("workspace", workspace, None, 0))
+    dev = next((t.device for _, t, _, _ in want if t is not None), None)
+    for name, t, dtype, n in want:
+        if t is None:
+            continue
+        bad = []
+        if not t.is_cuda:
+            bad.append(f"on {t.device}, not a CUDA device")
+        elif t.device != dev:
+            bad.append(f"on {t.device}, the other buffers on {dev}")
+        if dtype is not None and t.dtype != dtype:
+            bad.append(f"dtype {t.dtype}, want {dtype}")
+        if not t.is_contiguous():
+            bad.append("not contiguous")
+        if t.numel() < n:
+            bad.append(f"{t.numel()} elements, want at least {n}")
+        if bad:
+            raise IndexerTopkError(STATUS_NAMES.get("ITK_ERR_INVALID_ARGUMENT", 1), f"{name}: " + "; ".join(bad))
 
 
 class Plan:
@@ -176,6 +207,7 @@ def indexer_topk_workspace_bytes(plan: Plan) -> int:
 
 def indexer_topk_run(plan: Plan, q, k, w, out_ids, out_scores, workspace, stream=None):
     """q BF16 [T,64,128], k BF16 [Tkv,128], w FP32 [T,64], out_ids INT32 [T,top_k], out_scores FP32 [T,top_k]."""
+    _check_buffers(plan.desc, q, k, w, out_ids, out_scores, workspace)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().indexer_topk_run(plan.handle, _ptr(q), _ptr(k), _ptr(w), _ptr(out_ids), _ptr(out_scores),
                                    _ptr(workspace), nbytes, _stream_handle(stream)))
@@ -186,6 +218,7 @@ def indexer_topk_eager_workspace_bytes(desc: Desc) -> int:
 
 
 def indexer_topk_eager(desc: Desc, q, k, w, out_ids, out_scores, workspace, stream=None):
+    _check_buffers(desc, q, k, w, out_ids, out_scores, workspace)
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().indexer_topk_eager(desc.ref(), _ptr(q), _ptr(k), _ptr(w), _ptr(out_ids), _ptr(out_scores),
                                      _ptr(workspace), nbytes, _stream_handle(stream)))
@@ -215,6 +248,7 @@ def indexer_topk_run_noalloc(desc: Desc, q, k, w, out_ids, out_scores, stream=No
     For callers that must not allocate device memory at call time, e.g. a runtime that has
     already reserved the device memory for its own pool. Calls share one scratch array, so
     calls that overlap on the GPU race; keep them on one stream or ordered."""
+    _check_buffers(desc, q, k, w, out_ids, out_scores)
     _check(load().indexer_topk_run_noalloc(desc.ref(), _ptr(q), _ptr(k), _ptr(w), _ptr(out_ids), _ptr(out_scores),
                                            _stream_handle(stream)))
 

@@ -44,6 +44,11 @@ def test_argument_errors(env):
     with pytest.raises(binding.IndexerTopkError) as e:
         binding.indexer_topk_run(plan, q, k, None, ids, sc, ws)
     assert e.value.status == binding.ITK_ERR_NULL_POINTER
+    # refused by the binding: a strided q and a BF16 w would be read as the wrong layout or type
+    for bad in ((q.transpose(1, 2), k, w), (q, k, w.to(torch.bfloat16))):
+        with pytest.raises(binding.IndexerTopkError) as e:
+            binding.indexer_topk_run(plan, *bad, ids, sc, ws)
+        assert e.value.status == binding.ITK_ERR_INVALID_ARGUMENT
     plan.destroy()
     with pytest.raises(binding.IndexerTopkError) as e:
         binding.indexer_topk_prepare(wl.T, wl.Tkv, wl.cu_seqlens_q, wl.cu_seqlens_k, 4096)
