@@ -6,6 +6,7 @@ library offers indexer_topk_run_noalloc, whose scratch lives in one static devic
 This file is collected last so that a run that stops at the first failure has already
 run every other test; it also passes on its own in a fresh process.
 """
+import ctypes
 import numpy as np
 import pytest
 
@@ -71,9 +72,12 @@ def test_noalloc_rejects_too_many_units(env):
     binding, torch, dev = env
     T = 4 * 65536 + 4  # one work unit past the static scratch's unit table
     desc = binding.Desc(T, T, [0, T], [0, T], 8)
+    # through the C entry point itself, with dummy buffers: the unit count is refused
+    # before any buffer is read (the binding would refuse buffers this small first)
     e = torch.empty(16, dtype=torch.float32, device=dev)
+    p = ctypes.c_void_p(e.data_ptr())
     with pytest.raises(binding.IndexerTopkError) as err:
-        binding.indexer_topk_run_noalloc(desc, e, e, e, e, e)
+        binding._check(binding.load().indexer_topk_run_noalloc(desc.ref(), p, p, p, p, p, binding._stream_handle(None)))
     assert err.value.status == binding.ITK_ERR_UNSUPPORTED
     assert "static scratch" in str(err.value)
     assert binding.load().indexer_topk_noalloc_scratch_bytes() > 0
