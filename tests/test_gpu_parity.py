@@ -44,15 +44,17 @@ def binding(cuda_lib):
     return b
 
 
-def test_tiny_integer_bit_exact(binding, dev, oracle_mod):
-    wl = inputs.make("tiny", kind="int")
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_integer_bit_exact(binding, dev, oracle_mod, seed):
+    wl = inputs.make("tiny", kind="int", seed=seed)
     ids, sc = run_plan(binding, wl, dev)
     r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl))
     parity.assert_exact(ids, sc, r_ids, r_sc)
 
 
-def test_tiny_random_within_tolerance(binding, dev, oracle_mod):
-    wl = inputs.make("tiny")
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_random_within_tolerance(binding, dev, oracle_mod, seed):
+    wl = inputs.make("tiny", seed=seed)
     ids, sc = run_plan(binding, wl, dev)
     parity.assert_close(ids, sc, wl, np.arange(wl.T))
 
