@@ -352,6 +352,77 @@ __device__ __forceinline__ void warp_raise_threshold(uint32_t* qs, const uint32_
   }
 }
 
+// Raise a query's threshold bin as far as its histogram allows, by the whole group:
+// afterwards thr is the highest bin with at least K keys at or above it (it stays put while
+// fewer than K keys lie at or above it). qs: [0] count, [1] count at the last raise,
+// [2] threshold bin, [3] keys at or above the threshold bin. The histogram counts exactly
+// the buffer's keys in every bin at or above the current threshold: appends reach only
+// those bins, a compaction drops keys below it, and the exact path rebuilds the histogram.
+// Thread t holds bins [16 t, 16 t + 16) (bins below the threshold read as empty); a
+// reversed warp scan of the run sums and the four warp totals give the keys above each
+// run, and the one thread whose run crosses K walks its own bins. Called by every thread
+// of the group; the caller synchronizes the group before reading qs. It serves the first
+// raise of a unit, a walk from bin 0 across about a thousand bins; the later raises move
+// the threshold by a few bins and stay with warp_raise_threshold (one warp, faster there).
+__device__ __forceinline__ void group_raise_threshold(const GroupCtx& c, uint32_t* qs, const uint32_t* hist,
+                                                      uint32_t K) {
+  const uint32_t n = qs[0];
+  const uint32_t thr0 = qs[2];
+  const uint32_t ge0 = qs[3] + (n - qs[1]);  // keys at or above bin thr0
+  if (ge0 < K) {  // uniform: the threshold stays
+    gsync(c);     // every thread has read qs
+    if (c.gtid == 0) {
+      qs[1] = n;
+      qs[3] = ge0;
+    }
+    return;
+  }
+  const uint32_t b0 = 16u * static_cast<uint32_t>(c.gtid);
+  uint32_t h[16];
+  const uint4* run16 = reinterpret_cast<const uint4*>(hist + b0);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint4 x = run16[v];
+    h[4 * v + 0] = x.x;
+    h[4 * v + 1] = x.y;
+    h[4 * v + 2] = x.z;
+    h[4 * v + 3] = x.w;
+  }
+  uint32_t sum = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if (b0 + static_cast<uint32_t>(i) < thr0) h[i] = 0u;
+    sum += h[i];
+  }
+  uint32_t incl = sum;  // keys in this thread's run and the higher runs of its warp
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, incl, off);
+    if (c.lane + off < 32) incl += t;
+  }
+  if (c.lane == 0) c.radix[c.gwarp] = incl;  // the warp's total
+  gsync(c);                                  // (every thread has also read qs)
+  uint32_t above = incl - sum;               // keys in bins >= b0 + 16
+#pragma unroll
+  for (int w = 1; w < 4; ++w) above += w > c.gwarp ? c.radix[w] : 0u;
+  if (above < K && above + sum >= K) {  // exactly one thread: its run holds the new threshold
+    uint32_t run = above, thr = thr0, ge = ge0;
+    bool found = false;
+#pragma unroll
+    for (int i = 15; i >= 0; --i) {
+      run += h[i];
+      if (!found && run >= K) {
+        found = true;
+        thr = b0 + static_cast<uint32_t>(i);
+        ge = run;
+      }
+    }
+    qs[1] = n;
+    qs[2] = thr;
+    qs[3] = ge;
+  }
+}
+
 // ------------------------------------------------------------------ the kernel
 __global__ void __launch_bounds__(kNumThreads, 1)
     indexer_topk_scan_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
@@ -624,7 +695,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               break;
             }
             if (active) {
-              if (c.gwarp == 0) warp_raise_threshold(qs, hist_g, K, lane);
+              if (tile == kDenseTiles)  // the unit's first raise (uniform)
+                group_raise_threshold(c, qs, hist_g, K);
+              else if (c.gwarp == 0)
+                warp_raise_threshold(qs, hist_g, K, lane);
               gsync(c);
               // make room for the appends of the next kSyncEvery tiles (uniform decision)
               if (qs[0] > kCompactAt)
@@ -719,7 +793,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (direct) {
           if (c.gtid == 0) p.counts[item] = qs[0];  // every visible key, at most kCap
         } else {
-          if (c.gwarp == 0) warp_raise_threshold(qs, hist_g, K, lane);
+          if (no_sync)  // a unit without sync points: its first raise (uniform)
+            group_raise_threshold(c, qs, hist_g, K);
+          else if (c.gwarp == 0)
+            warp_raise_threshold(qs, hist_g, K, lane);
           gsync(c);
           epi_handoff(c, cand, qs, K, &s_pos[g], pol_cand, pol_store, p.store + item * kCap, p.counts + item, p.status);
         }
