@@ -2,15 +2,16 @@
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config S1]
 
-One step = one full scan (the indexer_topk_run call: one kernel) over the workload's
-synthetic inputs. The metric is effective TFLOP/s of useful causal MACs (2 * visible
-(query, key) pairs * H * D per call), with ms per call beside it. Inputs are resident
-in HBM; L2 is flushed between timed steps. Under torchrun each rank runs its own
-replica of the workload (seed + rank) on its own GPU: no collective touches the data
-path; the timing is reduced with a MAX over ranks.
+One step = one full scan, the indexer_topk_run call (the scan kernel, then the selection
+kernel -- or the merge kernel for split tails), over the workload's synthetic inputs. The
+metric is effective TFLOP/s of useful causal MACs (2 * visible (query, key) pairs * H * D
+per call), with ms per call (median over the timed steps) beside it. Inputs are resident
+in HBM; L2 is flushed between timed steps. Under torchrun each rank runs its own replica
+of the workload (seed + rank) on its own GPU: no collective touches the data path; the
+timing is reduced with a MAX over ranks.
 
 `--impl reference` times the CPU oracle (test infrastructure) on the host cores on a
-bounded sample of the same workload.
+bounded sample of the same workload; its per-call figure is extrapolated from the sample.
 """
 from __future__ import annotations
 
@@ -94,6 +95,14 @@ def load_traffic():
     return d
 
 
+def pci_bus_id(props):
+    """nvidia-smi's name of a CUDA device ("00000000:1B:00.0"), from its properties."""
+    try:
+        return f"{int(props.pci_domain_id):08X}:{int(props.pci_bus_id):02X}:{int(props.pci_device_id):02X}.0"
+    except (AttributeError, TypeError, ValueError):
+        return None
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples taken while the timed region runs."""
 
@@ -102,8 +111,11 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     PERIOD_MS = 50
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, bus_id: str | None = None):
+        # nvidia-smi numbers the physical GPUs and ignores CUDA_VISIBLE_DEVICES: name the
+        # device by its PCI bus id when it is known, so that the samples are of this GPU
         self.gpu = gpu_index
+        self.bus_id = bus_id
         self.proc = None
         # raw samples: $ITK_CLOCKS_DIR if set, else the temporary directory
         out_dir = os.environ.get("ITK_CLOCKS_DIR") or tempfile.gettempdir()
@@ -114,7 +126,7 @@ class ClockSampler:
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.bus_id or self.gpu}", f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
@@ -184,7 +196,8 @@ class ClockSampler:
         reasons = set().union(*[x[3] for x in samples_used])
         return {"sm_mhz": float(np.median([x[1] for x in samples_used])),
                 "sm_max_mhz": float(max(x[2] for x in samples_used)), "reasons": sorted(reasons),
-                "samples": len(samples_used), "window": window, "period_ms": self.PERIOD_MS}
+                "samples": len(samples_used), "window": window, "period_ms": self.PERIOD_MS,
+                "gpu": self.bus_id or f"index {self.gpu}"}
 
 
 def cpu_oracle_sample(wl, budget_s: float, seed_rows: int = 32):
@@ -252,13 +265,15 @@ def run_reference(args):
         t0 = time.perf_counter()
         oracle.topk(p, rows=rows)
         times.append(time.perf_counter() - t0)
-    t = float(np.mean(times))
+    t = float(np.median(times))
     value = flops / t / 1e12
     full_flops = 2.0 * visible_pairs(wl) * wl.H * wl.D
     sample = f"{len(rows)} of {wl.T} query rows, evenly spaced ({flops / full_flops:.4%} of the call's MACs)"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": full_flops / (value * 1e12) * 1e3,
+        "ms_per_step_kind": "extrapolated: the whole call's MACs at the sample's measured rate",
+        "sample_ms_per_step": t * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(wl, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
@@ -283,8 +298,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="S1")
-    ap.add_argument("--per-config", default="S2,C1,Z2,Z3,A1,A2,A3", help="extra configs timed and reported in per_config ('' = none)")
+    ap.add_argument("--per-config", default="tiny,S2,C1,Z2,Z3,A1,A2,A3",
+                    help="extra configs timed and reported in per_config ('' = none)")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-budget-per-config", type=float, default=3.0,
+                    help="seconds of oracle work for each per_config cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=20.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--residency", action="store_true",
@@ -347,13 +365,14 @@ def _timed_steps(binding, torch, plan, bufs, stream, steps, flush_buf, split=Fal
 
 
 def _step_ms(starts, splits, ends):
+    """Median over the timed steps of the whole call, and (with splits) of its two parts."""
     ends[-1].synchronize()
     total = np.array([a.elapsed_time(b) for a, b in zip(starts, ends)])
     if splits is None:
-        return float(total.mean()), None, None
+        return float(np.median(total)), None, None
     scan = np.array([a.elapsed_time(b) for a, b in zip(starts, splits)])
     sel = np.array([a.elapsed_time(b) for a, b in zip(splits, ends)])
-    return float(total.mean()), float(scan.mean()), float(sel.mean())
+    return float(np.median(total)), float(np.median(scan)), float(np.median(sel))
 
 
 def _e2e(binding, torch, wl, plan, bufs, stream, args, flush_buf, flops, world, dist, dev):
@@ -390,7 +409,7 @@ def _e2e(binding, torch, wl, plan, bufs, stream, args, flush_buf, flops, world, 
         if i >= args.warmup:
             e_e[i - args.warmup].record(stream)
     torch.cuda.synchronize()
-    serial_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in zip(e_s, e_e)])), dist, dev)
+    serial_ms = max_over_ranks(float(np.median([a.elapsed_time(b) for a, b in zip(e_s, e_e)])), dist, dev)
 
     # pipelined: copy-in stream, compute stream, copy-out stream, two buffer sets
     dq = [q, torch.empty_like(q)]
@@ -519,7 +538,8 @@ def run_ours(args):
 
     wl = inputs.make(args.config, seed=rank)
     flops = 2.0 * visible_pairs(wl) * wl.H * wl.D
-    clocks = ClockSampler(local).__enter__()  # sampling covers warm-up through the per-config runs
+    clocks = ClockSampler(local, pci_bus_id(torch.cuda.get_device_properties(dev))).__enter__()
+    # (sampling covers warm-up through the per-config runs)
     plan, bufs, stream = _measure(binding, torch, wl, dev, args.steps, args.warmup, flush_buf)
     q, k, w, ids, sc, ws = bufs
 
@@ -554,6 +574,7 @@ def run_ours(args):
         e2e = _e2e(binding, torch, wl, plan, bufs, stream, args, flush_buf, flops, world, dist, dev)
 
     # per-config figures (same method; parity-test configs, reported for the roofline)
+    traffic = load_traffic()
     per_config = {}
     for name in [c for c in args.per_config.split(",") if c and c != args.config]:
         wl2 = inputs.make(name, seed=rank)
@@ -565,11 +586,18 @@ def run_ours(args):
         plan2.device_status()
         tf2 = f2 / (m2 * 1e-3) / 1e12
         tf2_scan = f2 / (m2_scan * 1e-3) / 1e12
-        per_config[name] = {"ms": m2, "tflops": tf2, "frac": tf2 / peaks["bf16_tflops"],
-                            "scan_ms": m2_scan, "scan_frac": tf2_scan / peaks["bf16_tflops"], "finish_ms": m2_sel,
-                            "finish": finish_kernels(binding, wl2), "T": wl2.T, "Tkv": wl2.Tkv}
+        pc = {"ms": m2, "tflops": tf2, "frac": tf2 / peaks["bf16_tflops"],
+              "scan_ms": m2_scan, "scan_tflops": tf2_scan, "scan_frac": tf2_scan / peaks["bf16_tflops"],
+              "finish_ms": m2_sel, "finish": finish_kernels(binding, wl2), "T": wl2.T, "Tkv": wl2.Tkv,
+              "top_k": wl2.top_k, "gflop": f2 / 1e9,
+              "scan_traffic_bytes": None if traffic is None else traffic.get("per_config_bytes", {}).get(name)}
         plan2.destroy()
         del b2
+        if rank == 0 and args.cpu_budget_per_config > 0:
+            fs, ds, nr, th = cpu_oracle_sample(wl2, args.cpu_budget_per_config)
+            pc["cpu_baseline"] = {"value": fs / ds / 1e12, "unit": "TFLOP/s", "cores": th, "kind": "oracle",
+                                  "sample": f"{nr} of {wl2.T} query rows, evenly spaced; {ds:.1f} s"}
+        per_config[name] = pc
 
     clocks.__exit__(None, None, None)
     if rank != 0:
@@ -579,7 +607,6 @@ def run_ours(args):
 
     finish = [{"merge": "merge", "selection": "select"}[f] for f in finish_kernels(binding, wl).split(" + ")]
     achieved = flops / (scan_ms * 1e-3) / 1e12  # the dominant kernel alone
-    traffic = load_traffic()
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"],
                 "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)" if peak_src == "measured"

@@ -35,6 +35,7 @@ class _Desc(ctypes.Structure):
         ("cu_seqlens_q", ctypes.c_void_p),
         ("cu_seqlens_k", ctypes.c_void_p),
         ("q_causal_offsets", ctypes.c_void_p),
+        ("key_id_base", ctypes.c_int32),
     ]
 
 
@@ -84,6 +85,8 @@ def load():
         "indexer_topk_debug_inject": (ctypes.c_int, [vp, ctypes.c_int, vp]),
         "indexer_topk_run_noalloc": (ctypes.c_int, [DP, vp, vp, vp, vp, vp, vp]),
         "indexer_topk_noalloc_scratch_bytes": (sz, []),
+        "indexer_topk_noalloc_device_status": (ctypes.c_int, [vp]),
+        "indexer_topk_eager_device_status": (ctypes.c_int, [DP, vp, sz, vp]),
         "indexer_topk_set_split_event": (ctypes.c_int, [vp, vp]),
         "indexer_topk_bench_hold": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, vp]),
     }
@@ -107,15 +110,16 @@ def _check(rc: int):
 class Desc:
     """Host descriptor; keeps the int32 arrays alive while the C side may read them."""
 
-    def __init__(self, T, Tkv, cu_seqlens_q, cu_seqlens_k, top_k, q_causal_offsets=None, H=64, D=128):
+    def __init__(self, T, Tkv, cu_seqlens_q, cu_seqlens_k, top_k, q_causal_offsets=None, H=64, D=128, key_id_base=0):
         import numpy as np
 
         self.cu_q = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
         self.cu_k = np.ascontiguousarray(cu_seqlens_k, dtype=np.int32)
         self.offs = None if q_causal_offsets is None else np.ascontiguousarray(q_causal_offsets, dtype=np.int32)
         self.c = _Desc(int(T), int(Tkv), int(H), int(D), int(top_k), len(self.cu_q) - 1, self.cu_q.ctypes.data,
-                       self.cu_k.ctypes.data, None if self.offs is None else self.offs.ctypes.data)
+                       self.cu_k.ctypes.data, None if self.offs is None else self.offs.ctypes.data, int(key_id_base))
         self.T, self.Tkv, self.top_k, self.H, self.D = int(T), int(Tkv), int(top_k), int(H), int(D)
+        self.key_id_base = int(key_id_base)
 
     def ref(self):
         return ctypes.byref(self.c)
@@ -133,12 +137,20 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
+def _current_cuda_device():
+    """The CUDA device the library will launch on (the calling thread's current device)."""
+    import torch
+
+    return torch.device("cuda", torch.cuda.current_device())
+
+
 def _check_buffers(desc: Desc, q, k, w, out_ids, out_scores, workspace=None):
     """The checks the C ABI cannot make on plain pointers: every tensor given is a
-    contiguous CUDA tensor of the expected dtype, on q's device, holding at least the
-    elements the call reads or writes (a flat buffer is fine: the library reads rows of
-    H*D, D and H elements and writes rows of top_k). A missing buffer (None) is left to the
-    library, which reports ITK_ERR_NULL_POINTER; alignment is checked there too."""
+    contiguous CUDA tensor of the expected dtype, on the current CUDA device (the library
+    launches there, on that device's stream), holding at least the elements the call reads
+    or writes (a flat buffer is fine: the library reads rows of H*D, D and H elements and
+    writes rows of top_k). A missing buffer (None) is left to the library, which reports
+    ITK_ERR_NULL_POINTER; alignment is checked there too."""
     import torch
 
     T, Tkv, K, H, D = desc.T, desc.Tkv, desc.top_k, desc.H, desc.D
@@ -146,6 +158,12 @@ def _check_buffers(desc: Desc, q, k, w, out_ids, out_scores, workspace=None):
             ("out_ids", out_ids, torch.int32, T * K), ("out_scores", out_scores, torch.float32, T * K),
             ("workspace", workspace, None, 0))
     dev = next((t.device for _, t, _, _ in want if t is not None), None)
+    if dev is not None and dev.type == "cuda":
+        cur = _current_cuda_device()
+        if dev != cur:
+            raise IndexerTopkError(STATUS_NAMES.get("ITK_ERR_INVALID_ARGUMENT", 1),
+                                   f"buffers on {dev}, but the current CUDA device is {cur}: the library launches "
+                                   "on the current device (use torch.cuda.device(...) around the call)")
     for name, t, dtype, n in want:
         if t is None:
             continue
@@ -197,8 +215,8 @@ class Plan:
 
 
 def indexer_topk_prepare(T, Tkv, cu_seqlens_q, cu_seqlens_k, top_k, q_causal_offsets=None, H=64, D=128,
-                         stream=None) -> Plan:
-    return Plan(Desc(T, Tkv, cu_seqlens_q, cu_seqlens_k, top_k, q_causal_offsets, H, D), stream)
+                         stream=None, key_id_base=0) -> Plan:
+    return Plan(Desc(T, Tkv, cu_seqlens_q, cu_seqlens_k, top_k, q_causal_offsets, H, D, key_id_base), stream)
 
 
 def indexer_topk_workspace_bytes(plan: Plan) -> int:
@@ -222,6 +240,13 @@ def indexer_topk_eager(desc: Desc, q, k, w, out_ids, out_scores, workspace, stre
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().indexer_topk_eager(desc.ref(), _ptr(q), _ptr(k), _ptr(w), _ptr(out_ids), _ptr(out_scores),
                                      _ptr(workspace), nbytes, _stream_handle(stream)))
+
+
+def indexer_topk_eager_device_status(desc: Desc, workspace, stream=None):
+    """Raise if an eager call with this descriptor and workspace gave up a bounded wait or
+    failed an internal check (reads and clears the status word kept in the workspace)."""
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().indexer_topk_eager_device_status(desc.ref(), _ptr(workspace), nbytes, _stream_handle(stream)))
 
 
 def indexer_topk_validate(desc: Desc) -> int:
@@ -253,6 +278,12 @@ def indexer_topk_run_noalloc(desc: Desc, q, k, w, out_ids, out_scores, stream=No
                                            _stream_handle(stream)))
 
 
+def indexer_topk_noalloc_device_status(stream=None):
+    """Raise if the last no-allocation call on the current device gave up a bounded wait or
+    failed an internal check (reads and clears the status word of the static scratch)."""
+    _check(load().indexer_topk_noalloc_device_status(_stream_handle(stream)))
+
+
 def indexer_topk_set_split_event(plan: Plan, event=None):
     """Record `event` (a torch.cuda.Event that has been recorded once, or a raw
     cudaEvent_t handle) between the scan and the selection launch of later runs; None
@@ -266,16 +297,18 @@ def indexer_topk_bench_hold(n_ctas: int, microseconds: int, stream=None):
     _check(load().indexer_topk_bench_hold(int(n_ctas), int(microseconds), _stream_handle(stream)))
 
 
-def indexer_topk_debug_inject(plan: Plan, what: int, stream=None):
-    _check(load().indexer_topk_debug_inject(plan.handle, int(what), _stream_handle(stream)))
+def indexer_topk_debug_inject(plan, what: int, stream=None):
+    """Test hook (see the header); plan None targets the next no-allocation call (what = 5)."""
+    handle = None if plan is None else plan.handle
+    _check(load().indexer_topk_debug_inject(handle, int(what), _stream_handle(stream)))
 
 
-def indexer_topk(q, k, w, cu_seqlens_q, cu_seqlens_k, top_k, q_causal_offsets=None, stream=None):
+def indexer_topk(q, k, w, cu_seqlens_q, cu_seqlens_k, top_k, q_causal_offsets=None, stream=None, key_id_base=0):
     """One-shot scan through the eager entry; allocates outputs and workspace with torch."""
     import torch
 
     T, Tkv = q.shape[0], k.shape[0]
-    desc = Desc(T, Tkv, cu_seqlens_q, cu_seqlens_k, top_k, q_causal_offsets, q.shape[1], q.shape[2])
+    desc = Desc(T, Tkv, cu_seqlens_q, cu_seqlens_k, top_k, q_causal_offsets, q.shape[1], q.shape[2], key_id_base)
     ids = torch.empty((T, top_k), dtype=torch.int32, device=q.device)
     scores = torch.empty((T, top_k), dtype=torch.float32, device=q.device)
     ws = torch.empty(max(indexer_topk_eager_workspace_bytes(desc), 1), dtype=torch.uint8, device=q.device)

@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -45,6 +46,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 // Validated copy of a descriptor plus its work tables.
 struct Layout {
   int32_t T = 0, Tkv = 0, top_k = 0, B = 0;
+  int32_t key_id_base = 0;         // added to every returned id
   std::vector<UnitDesc> units;     // ticket order: most key tiles first
   std::vector<int32_t> item_rows;  // per store slot: output row, or -1 (empty or merged elsewhere)
   std::vector<itk::MergeDesc> merges;
@@ -71,6 +73,9 @@ int build_layout(const itk_desc* d, Layout* out) {
   if (d->top_k > itk::kMaxTopK) return fail(ITK_ERR_UNSUPPORTED, "top_k=%d exceeds %d", d->top_k, itk::kMaxTopK);
   if (static_cast<int64_t>(d->T) * itk::kHeads >= (int64_t(1) << 31))
     return fail(ITK_ERR_UNSUPPORTED, "T=%d too large (T*H must stay below 2^31)", d->T);
+  if (d->key_id_base < 0 || static_cast<int64_t>(d->key_id_base) + d->Tkv > INT32_MAX)
+    return fail(ITK_ERR_INVALID_ARGUMENT, "key_id_base=%d: ids key_id_base .. key_id_base + Tkv - 1 must lie in 0 .. 2^31-1",
+                d->key_id_base);
   const int B = d->num_segments;
   if (B == 0) {
     if (d->T != 0) return fail(ITK_ERR_INVALID_SEQLENS, "no segments but T=%d", d->T);
@@ -82,6 +87,7 @@ int build_layout(const itk_desc* d, Layout* out) {
   L.Tkv = d->Tkv;
   L.top_k = d->top_k;
   L.B = B;
+  L.key_id_base = d->key_id_base;
   if (B > 0) {
     const int32_t* cq = d->cu_seqlens_q;
     const int32_t* ck = d->cu_seqlens_k;
@@ -332,9 +338,17 @@ int check_run_buffers(const Layout& L, const void* q, const void* k, const float
 // Encode maps and launch the scan over the units of `t`, then the merge of split queries
 // (if any) and the selection of every slot with an output row (if any). `work` is laid
 // out by work_layout(grid, t.n_slots).
+// Test hooks of one run (indexer_topk_debug_inject).
+struct RunHooks {
+  bool force_launch_failure = false;  // the scan launch is refused by the runtime
+  bool static_schedule = false;       // fixed units per CTA instead of the ticket
+  bool withhold_timeout = false;      // CTA 0 withholds a key-tile load; waits limited to kShortWaitCycles
+};
+constexpr long long kShortWaitCycles = 1ll << 21;  // about 1 ms at 2 GHz
+
 int launch_run(const Layout& L, int grid, int sm_count, const RunTables& t, const void* q, const void* k,
                const float* w, int32_t* ids, float* scores, void* work, cudaStream_t stream,
-               bool force_launch_failure, cudaEvent_t split_event = nullptr, bool static_schedule = false) {
+               const RunHooks& hooks = RunHooks(), cudaEvent_t split_event = nullptr) {
   CUtensorMap qmap, kmap;
   int rc = encode_rows(&qmap, q, static_cast<uint64_t>(L.T) * itk::kHeads, itk::kN);
   if (rc) return rc;
@@ -354,10 +368,12 @@ int launch_run(const Layout& L, int grid, int sm_count, const RunTables& t, cons
   prm.cand = reinterpret_cast<unsigned long long*>(wb + wl.cand_off);
   prm.store = reinterpret_cast<unsigned long long*>(wb + wl.store_off);
   prm.counts = reinterpret_cast<uint32_t*>(wb + wl.counts_off);
-  prm.static_schedule = static_schedule ? 1 : 0;
+  prm.static_schedule = hooks.static_schedule ? 1 : 0;
+  prm.withhold_first_tile = hooks.withhold_timeout ? 1 : 0;
+  prm.wait_limit = hooks.withhold_timeout ? kShortWaitCycles : itk::kWaitLimitCycles;
   // A test hook asks for a launch the runtime must refuse: a dynamic shared-memory request
   // above the device limit is rejected at launch time and no work reaches the GPU.
-  const size_t smem = force_launch_failure ? size_t(1) << 30 : itk::kSmemBytes;
+  const size_t smem = hooks.force_launch_failure ? size_t(1) << 30 : itk::kSmemBytes;
   cudaError_t e = launch_dependent(itk::indexer_topk_scan_kernel, grid, itk::kNumThreads, smem, stream, qmap, kmap, prm);
   if (e != cudaSuccess) return cuda_fail(e, "scan launch");
   if (split_event) {
@@ -374,6 +390,7 @@ int launch_run(const Layout& L, int grid, int sm_count, const RunTables& t, cons
     mp.status = t.status;
     mp.out_ids = ids;
     mp.out_scores = scores;
+    mp.key_id_base = static_cast<uint32_t>(L.key_id_base);
     e = launch_dependent(itk::indexer_topk_merge_kernel, static_cast<int>(t.n_merges) * itk::kMergeCluster,
                          itk::kMergeThreads, itk::kMergeSmemBytes, stream, mp);
     if (e != cudaSuccess) return cuda_fail(e, "merge launch");
@@ -389,6 +406,7 @@ int launch_run(const Layout& L, int grid, int sm_count, const RunTables& t, cons
   sp.counts = prm.counts;
   sp.out_ids = ids;
   sp.out_scores = scores;
+  sp.key_id_base = static_cast<uint32_t>(L.key_id_base);
   const size_t items = t.n_slots;
   const int sel_grid = static_cast<int>(
       std::max<size_t>(1, std::min<size_t>(static_cast<size_t>(sm_count), (items + itk::kSelGroups - 1) / itk::kSelGroups)));
@@ -396,6 +414,28 @@ int launch_run(const Layout& L, int grid, int sm_count, const RunTables& t, cons
   if (e != cudaSuccess) return cuda_fail(e, "selection launch");
   return ITK_OK;
 }
+
+// Waits for `stream`, reads the device status word at d_status and clears it; maps a
+// nonzero word to ITK_ERR_INTERNAL or ITK_ERR_DEVICE_TIMEOUT (and sets *dirty). Allocates
+// nothing: the word goes to a host stack variable through a pageable copy.
+int read_status_word(uint32_t* d_status, cudaStream_t s, bool* dirty) {
+  uint32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, d_status, sizeof word, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  if (word == 0) return ITK_OK;
+  e = cudaMemsetAsync(d_status, 0, sizeof word, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (dirty) *dirty = true;
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
+  if ((word & 0xFFu) == itk::kStatusInternal)
+    return fail(ITK_ERR_INTERNAL, "device status word 0x%x (check %u failed)", word, (word >> 8) & 0xFFu);
+  return fail(ITK_ERR_DEVICE_TIMEOUT, "device status word 0x%x (wait in role %u gave up)", word, (word >> 8) & 0xFFu);
+}
+
+// debug_inject 5 with no plan: the next no-allocation call on this thread runs with the
+// withheld key tile and short wait limit.
+thread_local bool g_noalloc_timeout_next = false;
 
 }  // namespace
 
@@ -407,6 +447,7 @@ struct itk_plan_s {
   BlockLayout bl;
   bool ticket_dirty = false;
   bool fail_next_launch = false;  // test hook
+  bool timeout_next_run = false;  // test hook (debug_inject 5)
   cudaEvent_t split_event = nullptr;  // recorded between the two launches when set
   bool static_schedule = false;       // benchmark aid (debug_inject 3 / 4)
 };
@@ -521,10 +562,14 @@ int indexer_topk_run(itk_plan plan, const void* q, const void* k, const float* w
     cudaError_t e = cudaMemsetAsync(ticket, 0, 2 * sizeof(TicketBlock), s);
     if (e != cudaSuccess) return cuda_fail(e, "zeroing the ticket blocks");
   }
-  const bool inject = plan->fail_next_launch;
+  RunHooks hooks;
+  hooks.force_launch_failure = plan->fail_next_launch;
+  hooks.static_schedule = plan->static_schedule;
+  hooks.withhold_timeout = plan->timeout_next_run;
   plan->fail_next_launch = false;
+  plan->timeout_next_run = false;
   rc = launch_run(L, plan->grid, plan->dev.sm_count, block_tables(L, plan->bl, blk), q, k, w, out_ids, out_scores,
-                  workspace, s, inject, plan->split_event, plan->static_schedule);
+                  workspace, s, hooks, plan->split_event);
   plan->ticket_dirty = (rc != ITK_OK);
   return rc;
 }
@@ -562,8 +607,24 @@ int indexer_topk_eager(const itk_desc* desc, const void* q, const void* k, const
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(blk, host.data(), bl.bytes, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "uploading the eager unit table");
-  return launch_run(L, grid, dev.sm_count, block_tables(L, bl, blk), q, k, w, out_ids, out_scores, workspace, s,
-                    false);
+  return launch_run(L, grid, dev.sm_count, block_tables(L, bl, blk), q, k, w, out_ids, out_scores, workspace, s);
+}
+
+int indexer_topk_eager_device_status(const itk_desc* desc, void* workspace, size_t workspace_bytes, void* stream) {
+  Layout L;
+  int rc = build_layout(desc, &L);
+  if (rc) return rc;
+  if (L.T == 0) return ITK_OK;  // such a call ran nothing
+  DeviceInfo dev;
+  rc = query_device(&dev);
+  if (rc) return rc;
+  if (!workspace) return fail(ITK_ERR_NULL_POINTER, "workspace is NULL");
+  const size_t cand = work_layout(grid_for(L.units.size(), dev.sm_count), L.n_slots()).bytes;
+  const BlockLayout bl = block_layout(L);
+  if (workspace_bytes < cand + bl.bytes)
+    return fail(ITK_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu bytes", workspace_bytes, cand + bl.bytes);
+  return read_status_word(reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + cand + bl.status_off),
+                          static_cast<cudaStream_t>(stream), nullptr);
 }
 
 void indexer_topk_destroy(itk_plan plan) {
@@ -574,28 +635,21 @@ void indexer_topk_destroy(itk_plan plan) {
 
 int indexer_topk_device_status(itk_plan plan, void* stream) {
   if (!plan) return fail(ITK_ERR_INVALID_ARGUMENT, "plan is NULL");
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint32_t word = 0;
   uint32_t* d_status = reinterpret_cast<uint32_t*>(static_cast<char*>(plan->block) + plan->bl.status_off);
-  cudaError_t e = cudaMemcpyAsync(&word, d_status, sizeof word, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
-  if (word == 0) return ITK_OK;
-  e = cudaMemsetAsync(d_status, 0, sizeof word, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  plan->ticket_dirty = true;  // a run that gave up may have left the ticket blocks nonzero
-  if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
-  if ((word & 0xFFu) == itk::kStatusInternal)
-    return fail(ITK_ERR_INTERNAL, "device status word 0x%x (check %u failed)", word, (word >> 8) & 0xFFu);
-  return fail(ITK_ERR_DEVICE_TIMEOUT, "device status word 0x%x (wait in role %u gave up)", word, (word >> 8) & 0xFFu);
+  // a run that gave up may have left the ticket blocks nonzero: the next run zeroes them
+  return read_status_word(d_status, static_cast<cudaStream_t>(stream), &plan->ticket_dirty);
 }
 
 // ---------------------------------------------------------------- test hooks
-// Not part of the operation; used by the host-side recovery tests.
+// Not part of the operation; used by the recovery tests and the benchmark.
 //   what = 1: the next run's launch is refused by the runtime (oversized shared-memory
 //             request), as after a run that raised while launching.
 //   what = 2: write a nonzero value into the plan's two ticket blocks on `stream`, as a
 //             run that stopped midway would leave them.
+//   what = 3 / 4: fixed units per scan CTA / the ticket again.
+//   what = 5: the next run (plan NULL: the next no-allocation call of this thread) has
+//             CTA 0 withhold one key-tile load and every wait limited to kShortWaitCycles,
+//             so that the bounded waits run out and report a timeout.
 int indexer_topk_set_split_event(itk_plan plan, void* event) {
   if (!plan) return fail(ITK_ERR_INVALID_ARGUMENT, "plan is NULL");
   plan->split_event = static_cast<cudaEvent_t>(event);
@@ -603,6 +657,10 @@ int indexer_topk_set_split_event(itk_plan plan, void* event) {
 }
 
 int indexer_topk_debug_inject(itk_plan plan, int what, void* stream) {
+  if (what == 5 && !plan) {
+    g_noalloc_timeout_next = true;
+    return ITK_OK;
+  }
   if (!plan) return fail(ITK_ERR_INVALID_ARGUMENT, "plan is NULL");
   if (what == 1) {
     plan->fail_next_launch = true;
@@ -616,6 +674,10 @@ int indexer_topk_debug_inject(itk_plan plan, int what, void* stream) {
   }
   if (what == 3 || what == 4) {
     plan->static_schedule = (what == 3);
+    return ITK_OK;
+  }
+  if (what == 5) {
+    plan->timeout_next_run = true;
     return ITK_OK;
   }
   return fail(ITK_ERR_INVALID_ARGUMENT, "unknown injection %d", what);
@@ -740,6 +802,9 @@ int indexer_topk_run_noalloc(const itk_desc* desc, const void* q, const void* k,
   unsigned char* scratch = nullptr;
   rc = noalloc_scratch(dev.device, &scratch);
   if (rc) return rc;
+  RunHooks hooks;
+  hooks.withhold_timeout = g_noalloc_timeout_next;
+  g_noalloc_timeout_next = false;
   // The tables, then the ticket blocks and status word, which must start at zero: three
   // copies and one memset on the call's stream (the array keeps the previous call's
   // contents otherwise). Working buffers, store and counts need no clearing.
@@ -770,10 +835,26 @@ int indexer_topk_run_noalloc(const itk_desc* desc, const void* q, const void* k,
     // work_layout(grid, t.n_slots) of a chunk fits inside work_layout(kNoAllocMaxCtas, kNoAllocChunkSlots)
     const int grid = std::min(grid_for(n, dev.sm_count), kNoAllocMaxCtas);
     rc = launch_run(L, grid, std::min(dev.sm_count, kNoAllocMaxCtas), t, q, k, w, out_ids, out_scores, scratch, s,
-                    false);
+                    hooks);
     if (rc) return rc;
+    hooks.withhold_timeout = false;  // the hook covers the first launch pair
   }
   return ITK_OK;
+}
+
+int indexer_topk_noalloc_device_status(void* stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(ITK_ERR_NO_DEVICE, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(ITK_ERR_NO_DEVICE, "device ordinal %d out of range", dev);
+  unsigned char* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    scratch = static_cast<unsigned char*>(g_noalloc_ptr[dev]);
+  }
+  if (!scratch) return ITK_OK;  // no call has run on this device
+  return read_status_word(reinterpret_cast<uint32_t*>(scratch + kNoAllocStatusOff), static_cast<cudaStream_t>(stream),
+                          nullptr);
 }
 
 }  // extern "C"

@@ -2,9 +2,10 @@
 // tensor core (tcgen05: TMEM allocation, MMA, commit, TMEM loads) and cluster
 // barriers with distributed shared memory.
 //
-// Every wait here is bounded: it gives up after kWaitLimitCycles SM clocks (about one
-// second) or as soon as the CTA's abort flag is raised, and reports the give-up to the
-// caller, which then sets the device status word and unwinds. No wait can spin forever.
+// Every wait here is bounded: it gives up after a limit of SM clocks (kWaitLimitCycles,
+// about one second, unless the caller passes a shorter one) or as soon as the CTA's abort
+// flag is raised, and reports the give-up to the caller, which then sets the device status
+// word and unwinds. No wait can spin forever.
 #pragma once
 
 #include <cstdint>
@@ -49,14 +50,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed. Returns false if the wait
-// ran out of time or (when abort_flag is not null) the CTA abort flag was raised.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile uint32_t* abort_flag) {
+// ran out of time (`limit` SM clocks) or (when abort_flag is not null) the CTA abort flag
+// was raised.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile uint32_t* abort_flag,
+                                          long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (abort_flag && *abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
 }
 

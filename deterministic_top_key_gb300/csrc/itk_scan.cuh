@@ -105,6 +105,8 @@ struct ScanParams {
   unsigned long long* store;     // [n_units * 4][kCap] candidate keys handed to the selection kernel
   uint32_t* counts;              // [n_slots] keys in each store slot
   int32_t static_schedule;       // benchmark aid: 1 = CTA b takes units b, b + grid, ... (no ticket)
+  int32_t withhold_first_tile;   // test hook: 1 = CTA 0 never loads the first key tile of its first unit
+  long long wait_limit;          // SM clocks after which an in-kernel wait gives up (kWaitLimitCycles)
 };
 
 constexpr size_t kCandKeysPerCta = static_cast<size_t>(kQB) * kQCap + kEpiGroups * kMaxTopK;
@@ -498,7 +500,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                          ? static_cast<unsigned long long>(blockIdx.x) + it * gridDim.x
                                          : atomicAdd(&p.ticket->next, 1ull);
         const int slot = it & 1;
-        if (!mbar_wait(bars.ue(slot), ((it >> 1) & 1) ^ 1, s_abort)) {
+        if (!mbar_wait(bars.ue(slot), ((it >> 1) & 1) ^ 1, s_abort, p.wait_limit)) {
           record_timeout(p.status, s_abort, 1);
           break;
         }
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           grid_dep_launch_dependents();  // no unit left for this CTA: the next kernel may launch
           break;
         }
-        if (!mbar_wait(bars.qempty, (it & 1) ^ 1, s_abort)) {
+        if (!mbar_wait(bars.qempty, (it & 1) ^ 1, s_abort, p.wait_limit)) {
           record_timeout(p.status, s_abort, 2);
           break;
         }
@@ -529,11 +531,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         ++qloads;
         for (int tile = range.y; tile < range.z; ++tile, ++kc) {
           const int s = kc % kStages;
-          if (!mbar_wait(bars.ke(s), ((kc / kStages) & 1) ^ 1, s_abort)) {
+          if (!mbar_wait(bars.ke(s), ((kc / kStages) & 1) ^ 1, s_abort, p.wait_limit)) {
             record_timeout(p.status, s_abort, 3);
             ok = false;
             break;
           }
+          // test hook: the tile's barrier phase never completes, as if its load never arrived
+          if (p.withhold_first_tile && blockIdx.x == 0 && it == 0 && tile == range.y) continue;
           mbar_arrive_expect_tx(bars.kf(s), kKStageBytes);
           const uint32_t kdst = smem_u32(smem + kOffK + s * kKStageBytes);
           const int row = unit.z + tile * kBlockKeys;
@@ -545,8 +549,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       // Drain: no TMA write into this CTA's shared memory may still be in flight (these
       // waits ignore the abort flag but keep their time limit).
       for (uint32_t j = (kc > kStages ? kc - kStages : 0); j < kc; ++j)
-        mbar_wait(bars.kf(j % kStages), (j / kStages) & 1, nullptr);
-      if (qloads > 0) mbar_wait(bars.qfull, (qloads - 1) & 1, nullptr);
+        mbar_wait(bars.kf(j % kStages), (j / kStages) & 1, nullptr, p.wait_limit);
+      if (qloads > 0) mbar_wait(bars.qfull, (qloads - 1) & 1, nullptr, p.wait_limit);
       ticket_release(p.ticket);
     }
   } else if (warp == 1) {
@@ -558,26 +562,26 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool ok = true;
       while (ok) {
         const int slot = it & 1;
-        if (!mbar_wait(bars.uf(slot), (it >> 1) & 1, s_abort)) {
+        if (!mbar_wait(bars.uf(slot), (it >> 1) & 1, s_abort, p.wait_limit)) {
           record_timeout(p.status, s_abort, 4);
           break;
         }
         const int4 unit = s_unit[2 * slot];
         if (unit.x < 0) break;
-        if (!mbar_wait(bars.qfull, it & 1, s_abort)) {
+        if (!mbar_wait(bars.qfull, it & 1, s_abort, p.wait_limit)) {
           record_timeout(p.status, s_abort, 5);
           break;
         }
         const int nt = s_unit[2 * slot + 1].z - s_unit[2 * slot + 1].y;
         for (int tile = 0; tile < nt; ++tile, ++kc, ++ac) {
           const int ab = ac & 1;
-          if (!mbar_wait(bars.ae(ab), ((ac >> 1) & 1) ^ 1, s_abort)) {
+          if (!mbar_wait(bars.ae(ab), ((ac >> 1) & 1) ^ 1, s_abort, p.wait_limit)) {
             record_timeout(p.status, s_abort, 6);
             ok = false;
             break;
           }
           const int s = kc % kStages;
-          if (!mbar_wait(bars.kf(s), (kc / kStages) & 1, s_abort)) {
+          if (!mbar_wait(bars.kf(s), (kc / kStages) & 1, s_abort, p.wait_limit)) {
             record_timeout(p.status, s_abort, 7);
             ok = false;
             break;
@@ -604,7 +608,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       // Every MMA this thread issued completes before TMEM is released (ignores the
       // abort flag, keeps the time limit).
       mma_commit(bars.mmadone);
-      mbar_wait(bars.mmadone, 0, nullptr);
+      mbar_wait(bars.mmadone, 0, nullptr, p.wait_limit);
     }
   } else {
     // ---------------------------------------------------------------- epilogue
@@ -638,7 +642,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int slot = it & 1;
       // Every decision to leave the loop is taken by the whole group at once (flag set
       // before a group barrier, read after it), so no warp is left waiting at a barrier.
-      if (!mbar_wait(bars.uf(slot), (it >> 1) & 1, s_abort)) {
+      if (!mbar_wait(bars.uf(slot), (it >> 1) & 1, s_abort, p.wait_limit)) {
         record_timeout(p.status, s_abort, 8);
         atomicOr(&s_gfail[g], 1u);
       }
@@ -707,7 +711,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               thr_f = thr < 4u ? -__int_as_float(0x7F800000) : key_to_float(thr << kBinShift);
             }
           }
-          if (!mbar_wait(bars.af(ab), (ac >> 1) & 1, s_abort)) {
+          if (!mbar_wait(bars.af(ab), (ac >> 1) & 1, s_abort, p.wait_limit)) {
             record_timeout(p.status, s_abort, 10);
             atomicOr(&s_gfail[g], 1u);  // the group leaves at its next sync point
             continue;

@@ -67,6 +67,7 @@ struct SelectParams {
   const uint32_t* counts;             // [n_items] candidates per slot
   int32_t* out_ids;                   // [T, top_k]
   float* out_scores;                  // [T, top_k]
+  uint32_t key_id_base;               // added to every written id (the keys hold global key rows)
 };
 
 // Exclusive prefix sum of the padded array a (entry i at a[sub_pad(i)], i < n <= kSG *
@@ -193,7 +194,8 @@ __device__ __noinline__ void sel_crossing_fallback(const GroupCtx& c, const unsi
 // gtid + kSG r in registers.
 __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned long long* buf, uint32_t n,
                                            uint32_t top_k, uint32_t* ge, uint32_t* sub, unsigned long long* stage,
-                                           uint16_t* bkt, uint32_t* flags, int32_t* out_ids, float* out_scores) {
+                                           uint16_t* bkt, uint32_t* flags, int32_t* out_ids, float* out_scores,
+                                           uint32_t id_base) {
   unsigned long long vk[kSelPer];  // full 64-bit keys; the score word is the high half
   // entry r of this thread is candidate gtid + kSG r: it exists for r < ceil((n - gtid) / kSG)
   const uint32_t n_mine = n > static_cast<uint32_t>(c.gtid) ? (n - c.gtid + kSG - 1u) / kSG : 0u;
@@ -326,7 +328,7 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
         uint32_t pos = start[u];
         for (uint32_t i = start[u]; i < end[u]; ++i) pos += stage[i] > x[u] ? 1u : 0u;
         if (end[u] > start[u] && pos < keff) {
-          st_stream_s32(out_ids + pos, static_cast<int32_t>(static_cast<uint32_t>(x[u] & 0xFFFFFFFFull)));
+          st_stream_s32(out_ids + pos, static_cast<int32_t>(static_cast<uint32_t>(x[u] & 0xFFFFFFFFull) + id_base));
           st_stream_f32(out_scores + pos, key_to_float(static_cast<uint32_t>(x[u] >> 32)));
         }
       }
@@ -391,7 +393,7 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   for (uint32_t r = c.gtid; r < top_k; r += kSG) {
     if (r < keff) {
       const unsigned long long x = stage[r];
-      st_stream_s32(out_ids + r, static_cast<int32_t>(static_cast<uint32_t>(x & 0xFFFFFFFFull)));
+      st_stream_s32(out_ids + r, static_cast<int32_t>(static_cast<uint32_t>(x & 0xFFFFFFFFull) + id_base));
       st_stream_f32(out_scores + r, key_to_float(static_cast<uint32_t>(x >> 32)));
     } else {
       st_stream_s32(out_ids + r, -1);
@@ -453,7 +455,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) indexer_topk_select_kernel(con
       }
       const size_t row = static_cast<size_t>(out_row);
       sel_finish(c, p.store + item * kCap, n, static_cast<uint32_t>(p.top_k), ge, sub, stage, bkt, flags,
-                 p.out_ids + row * p.top_k, p.out_scores + row * p.top_k);
+                 p.out_ids + row * p.top_k, p.out_scores + row * p.top_k, p.key_id_base);
     }
     if (c.gtid == 0) publish(next);
     gsync(c);
@@ -505,6 +507,7 @@ struct MergeParams {
   uint32_t* status;
   int32_t* out_ids;     // [T, top_k]
   float* out_scores;    // [T, top_k]
+  uint32_t key_id_base; // added to every written id
 };
 
 // Adds one to h[d] for every lane with v; lanes with the same digit share one atomic.
@@ -764,7 +767,7 @@ __global__ void __cluster_dims__(kMergeCluster, 1, 1) __launch_bounds__(kMergeTh
       pos += lo - first;
     }
     if (pos < keff) {
-      st_stream_s32(out_ids + pos, static_cast<int32_t>(static_cast<uint32_t>(x & 0xFFFFFFFFull)));
+      st_stream_s32(out_ids + pos, static_cast<int32_t>(static_cast<uint32_t>(x & 0xFFFFFFFFull) + p.key_id_base));
       st_stream_f32(out_scores + pos, key_to_float(static_cast<uint32_t>(x >> 32)));
     }
   }

@@ -21,8 +21,8 @@
  *
  * Output of row t (our reading where the page is silent): k_eff = min(top_k, p + 1)
  * entries sorted by score descending, equal scores by id descending; slots k_eff ..
- * top_k-1 hold id -1 and score -INFINITY. Ids are global row indices into k. A score
- * of -0.0 is returned as +0.0.
+ * top_k-1 hold id -1 and score -INFINITY. The id of key row s is key_id_base + s
+ * (key_id_base = 0: global row indices into k). A score of -0.0 is returned as +0.0.
  *
  * Supported: H == 64, D == 128, 1 <= top_k <= 2048, any number of segments.
  *
@@ -90,6 +90,9 @@ typedef struct {
   const int32_t* cu_seqlens_q;     /* [B+1], cu_q[0] = 0, non-decreasing, cu_q[B] = T */
   const int32_t* cu_seqlens_k;     /* [B+1], cu_k[0] = 0, non-decreasing, cu_k[B] <= Tkv */
   const int32_t* q_causal_offsets; /* [B] or NULL (bottom-right: off_b = Tk_b - Tq_b) */
+  int32_t key_id_base;      /* added to every returned key id; 0 = global row ids into k.
+                               0 <= key_id_base <= 2^31 - 1 - Tkv, so ids stay non-negative
+                               int32 and keep their order (ITK_ERR_INVALID_ARGUMENT otherwise) */
 } itk_desc;
 
 /*
@@ -115,9 +118,13 @@ ITK_API size_t indexer_topk_workspace_bytes(itk_plan plan);
  * One scan on `stream`: two kernel launches -- the scan, which leaves each query's
  * candidates (a superset of its top-k, at most 4096 keys) in the workspace, then the
  * selection, which writes the sorted top-k rows. A split-tail descriptor (see
- * indexer_topk_unit_table) adds the merge, which selects and writes the rows of its split
- * queries from their chunks' candidates; the selection is left out when every query is
- * split. Plus a 32-byte memset only right after a failed launch. Arguments:
+ * indexer_topk_unit_table) launches, in place of the selection, the merge, which selects
+ * and writes the rows of its split queries from their chunks' candidates; a descriptor
+ * with both split and whole query blocks launches both (three kernels). The scan
+ * is always the first launch. No copy and no memset is issued, except one 32-byte memset
+ * right after a failed launch. (The page's scan is one kernel; here the selection is a
+ * kernel of its own, because run inside the scan kernel its warps took issue slots from
+ * the score epilogue.) Arguments:
  *   q          device, BF16 [T,H,D] row-major, 16-byte aligned
  *   k          device, BF16 [Tkv,D] row-major, 16-byte aligned
  *   w          device, FP32 [T,H] row-major
@@ -139,13 +146,25 @@ ITK_API int indexer_topk_run(itk_plan plan, const void* q, const void* k, const 
  * device memory: the unit table and the ticket blocks live at the end of the caller's
  * workspace, which must hold indexer_topk_eager_workspace_bytes(desc) bytes. Device work
  * on `stream`: one host-to-device copy of the unit table with zeroed ticket blocks, then
- * the scan and selection kernels. Reference: same page, "Changes" table row "Runner entry points and
+ * the kernels of indexer_topk_run (the scan first). Reference: same page, "Changes" table row "Runner entry points and
  * validation" (the eager entry uses a one-shot runner) and the TicketWord commit note (the
  * eager entry zeroes its ticket word on the launch stream).
  */
 ITK_API size_t indexer_topk_eager_workspace_bytes(const itk_desc* desc);
 ITK_API int indexer_topk_eager(const itk_desc* desc, const void* q, const void* k, const float* w, int32_t* out_ids,
                        float* out_scores, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Device status of eager calls that used this workspace: waits for `stream`, then reads and
+ * clears the status word that the eager entry keeps in the caller's workspace (at an offset
+ * that depends on `desc`, so pass the descriptor and workspace of the call). Returns ITK_OK,
+ * ITK_ERR_DEVICE_TIMEOUT or ITK_ERR_INTERNAL as indexer_topk_device_status does; a call that
+ * reported either has undefined outputs. Each eager call clears the word before it runs, so
+ * read it after the call whose outcome you need. ITK_ERR_WORKSPACE_TOO_SMALL if the
+ * workspace cannot be one of `desc`'s.
+ */
+ITK_API int indexer_topk_eager_device_status(const itk_desc* desc, void* workspace, size_t workspace_bytes,
+                                             void* stream);
 
 /* Release the plan's device block (synchronizes nothing; the caller must not destroy a
  * plan while one of its runs may still execute). NULL is ignored. */
@@ -203,9 +222,13 @@ ITK_API const char* indexer_topk_version(void);
  *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call. The
  *     work-unit table is copied from host memory and the ticket blocks and status word
  *     are zeroed on `stream` before the scan; working buffers and store need no clearing.
- *   - Limits: at most 65536 work units (4 consecutive queries of one segment each, so
- *     about 262144 queries), and at most 152 CTAs; larger descriptors are rejected with
- *     ITK_ERR_UNSUPPORTED and a message from indexer_topk_last_error().
+ *   - Limit: at most 65536 work units (4 consecutive queries of one segment each, so
+ *     about 262144 queries); a larger descriptor is rejected with ITK_ERR_UNSUPPORTED and
+ *     a message from indexer_topk_last_error(). The grids are capped at 152 CTAs, because
+ *     the static working buffers hold 152 scan CTAs; on a device with more SMs the calls
+ *     still run, on 152 of them.
+ *   - In-kernel wait timeouts and failed internal checks of a call are reported by
+ *     indexer_topk_noalloc_device_status(); the next call clears the word first.
  *   - The first call on a device looks up the array's device address (once per device,
  *     with that device current) -- make that first call before any stream capture.
  *   - Every call shares the one array and leaves its contents behind: calls that overlap
@@ -237,6 +260,15 @@ ITK_API int indexer_topk_bench_hold(int n_ctas, int microseconds, void* stream);
 ITK_API size_t indexer_topk_noalloc_scratch_bytes(void);
 
 /*
+ * Device status of the last indexer_topk_run_noalloc call on the current device: waits for
+ * `stream`, then reads and clears the status word in the static scratch array. ITK_OK, or
+ * ITK_ERR_DEVICE_TIMEOUT / ITK_ERR_INTERNAL as indexer_topk_device_status reports them (the
+ * outputs of that call are then undefined). Allocates nothing. ITK_OK if no call has run on
+ * this device yet.
+ */
+ITK_API int indexer_topk_noalloc_device_status(void* stream);
+
+/*
  * Test and benchmark hook; not part of the operation.
  *   what = 1: the next indexer_topk_run's launch is refused by the CUDA runtime (an
  *             oversized shared-memory request; no work reaches the GPU), as after a run
@@ -249,6 +281,14 @@ ITK_API size_t indexer_topk_noalloc_scratch_bytes(void);
  *             units). what = 4 restores the ticket.
  */
 ITK_API int indexer_topk_debug_inject(itk_plan plan, int what, void* stream);
+/*   what = 5: the next run of `plan` -- or, with plan NULL, the next indexer_topk_run_noalloc
+ *             call on this thread -- runs with every in-kernel wait limited to about 1 ms
+ *             (2^21 SM clocks), and scan CTA 0 withholds the first key-tile load of its
+ *             first unit, so that the waits on it run out as a load that never arrives
+ *             would make them: the CTA records ITK_ERR_DEVICE_TIMEOUT in the status word,
+ *             waits for its own copies and tensor-core work, frees its tensor memory and
+ *             returns. The call itself returns ITK_OK with undefined outputs; the status
+ *             readers report the timeout, and the next run is correct again. */
 
 #ifdef __cplusplus
 }

@@ -47,6 +47,10 @@ def test_validation(lib):
     assert binding.indexer_topk_validate(_desc(q_causal_offsets=[11])) == binding.ITK_ERR_INVALID_OFFSETS
     assert binding.indexer_topk_validate(_desc(q_causal_offsets=[-1])) == binding.ITK_ERR_INVALID_OFFSETS
     assert binding.indexer_topk_validate(_desc(q_causal_offsets=[10])) == 0
+    assert binding.indexer_topk_validate(_desc(key_id_base=5)) == 0
+    assert binding.indexer_topk_validate(_desc(key_id_base=2**31 - 1 - 20)) == 0  # last id 2^31 - 2
+    assert binding.indexer_topk_validate(_desc(key_id_base=2**31 - 20)) == binding.ITK_ERR_INVALID_ARGUMENT
+    assert binding.indexer_topk_validate(_desc(key_id_base=-1)) == binding.ITK_ERR_INVALID_ARGUMENT
     assert binding.indexer_topk_validate(
         _desc(T=4, cu_seqlens_q=[0, 4, 2], cu_seqlens_k=[0, 5, 6])) == binding.ITK_ERR_INVALID_SEQLENS
     assert lib.indexer_topk_validate(None) == binding.ITK_ERR_INVALID_ARGUMENT

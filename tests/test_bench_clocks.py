@@ -41,3 +41,15 @@ def test_short_region_falls_back_and_keeps_reasons(tmp_path):
     out = s.summary()
     assert out["window"].startswith("all GPU work")
     assert out["samples"] == 2 and out["reasons"] == ["sw_power_cap"]
+
+
+def test_sampler_names_the_gpu_by_pci_bus_id():
+    """nvidia-smi numbers physical GPUs and ignores CUDA_VISIBLE_DEVICES, so the sampler
+    asks for the CUDA device's PCI bus id, built from its properties."""
+    from types import SimpleNamespace
+
+    props = SimpleNamespace(pci_domain_id=0, pci_bus_id=0x1B, pci_device_id=0)
+    assert bench.pci_bus_id(props) == "00000000:1B:00.0"
+    assert bench.pci_bus_id(SimpleNamespace()) is None
+    s = bench.ClockSampler(3, "00000000:1B:00.0")
+    assert s.bus_id == "00000000:1B:00.0"

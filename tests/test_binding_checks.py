@@ -50,8 +50,15 @@ class _FakeCuda:
         return self.t.numel()
 
 
-def _fake(bufs):
-    return [_FakeCuda(t) for t in bufs]
+def _fake(bufs, device="cuda:0"):
+    return [_FakeCuda(t, device=device) for t in bufs]
+
+
+@pytest.fixture(autouse=True)
+def current_device_is_cuda0(monkeypatch):
+    """The library launches on the calling thread's current CUDA device; here that is a
+    stand-in for cuda:0 (no GPU on this host)."""
+    monkeypatch.setattr(binding, "_current_cuda_device", lambda: torch.device("cuda", 0))
 
 
 def test_well_formed_buffers_pass():
@@ -70,3 +77,10 @@ def test_wrong_dtype_layout_size_or_device_is_refused():
     _refused(_desc(), q, k, w, _FakeCuda(torch.zeros((6, 4), dtype=torch.int64)), sc, match="dtype")
     _refused(_desc(), q, k, w, ids, _FakeCuda(sc.t, device="cuda:1"), match="other buffers")
     _refused(_desc(top_k=8), q, k, w, ids, sc, match="want at least 48")
+
+
+def test_buffers_on_another_device_than_the_current_one_are_refused():
+    """Every buffer on cuda:1 while cuda:0 is current: the kernels would run on cuda:0 and
+    reach the buffers as peer pointers, so the binding refuses before the C call."""
+    _refused(_desc(), *_fake(_bufs(), device="cuda:1"), match="current CUDA device is cuda:0")
+    binding._check_buffers(_desc(), *_fake(_bufs(), device="cuda:0"))

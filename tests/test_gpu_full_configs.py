@@ -1,8 +1,13 @@
 """Full-size configurations, in the launch configuration the benchmark times.
 
 Every row is checked for validity (sorted by the total order, unique ids inside the
-query's visible range, fill after k_eff); sampled rows are checked against the oracle:
-bit-exact on the integer variant, within tolerance on the random inputs.
+query's visible range, fill after k_eff). Against the oracle: on the integer variant,
+every row of S1 and S2 and at least 512 rows of the others, bit-exact; on random inputs
+at least 512 rows per configuration (all rows of the split tails), within tolerance. The
+sampled rows cover every kind of work unit the scan runs -- queries that see at most 4096
+keys (appended straight to the store), at most 16384 (positional working buffer, one
+threshold raise) and more (filtered with sync points) -- and the first and last query of
+every segment.
 """
 import numpy as np
 import pytest
@@ -12,14 +17,29 @@ from tests import parity
 
 pytestmark = pytest.mark.gpu
 
+ALL_ROWS_INT = ("S1", "S2")  # the oracle runs every row of these in about 15 s and 60 s on 16 cores
 
-def _sample_rows(wl, n=40, seed=0):
+
+def _sample_rows(wl, n=512, seed=0):
+    """About n rows: the segment edges, then an even share of random rows from each kind
+    of unit (by the number of keys the query sees), all rows if T <= n."""
+    if wl.T <= n:
+        return np.arange(wl.T, dtype=np.int32)
     rng = np.random.default_rng(seed)
-    rows = set(rng.choice(wl.T, size=min(n, wl.T), replace=False).tolist())
+    _, vis = _row_visible(wl)
+    rows = set()
     for b in range(wl.num_segments):  # segment edges
         q0, q1 = int(wl.cu_seqlens_q[b]), int(wl.cu_seqlens_q[b + 1])
         if q1 > q0:
             rows.update({q0, q1 - 1})
+    kinds = [np.nonzero(vis <= 4096)[0], np.nonzero((vis > 4096) & (vis <= 16384))[0], np.nonzero(vis > 16384)[0]]
+    kinds = [x for x in kinds if len(x)]
+    per = max(1, (n - len(rows)) // len(kinds))
+    for x in kinds:
+        rows.update(rng.choice(x, size=min(per, len(x)), replace=False).tolist())
+    rest = np.setdiff1d(np.arange(wl.T), np.fromiter(rows, np.int64))
+    if len(rows) < n:  # top up with rows of any kind
+        rows.update(rng.choice(rest, size=min(n - len(rows), len(rest)), replace=False).tolist())
     return np.array(sorted(rows), np.int32)
 
 
@@ -96,6 +116,11 @@ def test_full_config_integer(name, dev, oracle_mod):
     wl = inputs.make(name, kind="int")
     ids, sc = _run(wl, dev)
     _check_all_rows(ids, sc, wl)
-    rows = _sample_rows(wl, n=24, seed=1)
-    r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl), rows=rows)
-    parity.assert_exact(ids, sc, r_ids, r_sc, rows=rows)
+    if name in ALL_ROWS_INT:
+        r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl))
+        parity.assert_exact(ids, sc, r_ids, r_sc)
+    else:
+        rows = _sample_rows(wl, seed=1)
+        assert len(rows) >= min(512, wl.T)
+        r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl), rows=rows)
+        parity.assert_exact(ids, sc, r_ids, r_sc, rows=rows)

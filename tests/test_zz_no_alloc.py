@@ -1,4 +1,5 @@
-"""The entry point that allocates nothing, checked against the prepared entry point.
+"""The entry point that allocates nothing, checked against the prepared entry point and,
+on integer inputs, against the oracle.
 
 Some callers cannot call cudaMalloc when they run the scan -- for example a serving
 runtime that has already reserved the device memory for its own pool. For them the
@@ -66,6 +67,34 @@ def test_noalloc_matches_prepared_on_two_calls(env):
         # the same kernel on the same inputs: identical bits, well within the tolerance
         # of the random-input parity tests
         parity.assert_exact(got_ids, got_sc, ref_ids, ref_sc)
+        binding.indexer_topk_noalloc_device_status()
+        if wl.meta["kind"] == "int":  # every FP32 sum exact: bit-identical to the oracle too
+            import oracle
+
+            o_ids, o_sc = oracle.topk(parity.oracle_problem(wl))
+            parity.assert_exact(got_ids, got_sc, o_ids, o_sc)
+
+
+def test_noalloc_reports_a_wait_timeout_then_runs_exact(env):
+    """A call whose scan CTA 0 withholds a key-tile load with every wait cut to about
+    1 ms (test hook): its status reader reports the timeout, which the call itself cannot
+    return (its kernels run after it returns), and the next call is exact again."""
+    binding, torch, dev = env
+    import oracle
+
+    wl = inputs.draw(300, 900, [0, 300], [0, 900], 128, seed=35, kind="int")
+    q, k, w = parity.to_device(wl, dev)
+    o_ids, o_sc = oracle.topk(parity.oracle_problem(wl))
+    binding.indexer_topk_debug_inject(None, 5)
+    _noalloc(binding, torch, dev, wl, q, k, w)
+    with pytest.raises(binding.IndexerTopkError) as err:
+        binding.indexer_topk_noalloc_device_status()
+    assert err.value.status == binding.ITK_ERR_DEVICE_TIMEOUT
+    binding.indexer_topk_noalloc_device_status()  # reading cleared the word
+    for _ in range(2):
+        got_ids, got_sc = _noalloc(binding, torch, dev, wl, q, k, w)
+        binding.indexer_topk_noalloc_device_status()
+        parity.assert_exact(got_ids, got_sc, o_ids, o_sc)
 
 
 def test_noalloc_rejects_too_many_units(env):
