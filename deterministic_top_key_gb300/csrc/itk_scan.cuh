@@ -30,7 +30,8 @@
 // s keeps eight partial sums p_m (m = 0..7), p_m = fma(w[t,h], max(x_h, 0), p_m) over
 // h = m, m+8, ..., m+56 in that order, and returns
 //     ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7)) + 0
-// (the "+ 0" turns a -0 into +0).
+// (the "+ 0" turns a -0 into +0). Chains 2..7 are evaluated on doubled values (relu_form,
+// pair_sum below) to share the work between two pipes; the result is the same bits.
 //
 // Candidate filter: a query's working buffer holds keys whose score key lies in a bin
 // (top 11 bits of the order-preserving score key) at or above a threshold bin; the
@@ -138,6 +139,21 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
       "mov.b64 {%0, %1}, c;\n\t}"
       : "+f"(d0), "+f"(d1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// ReLU of the chains of pair j (chains 2j and 2j + 1): max(x, 0), or x + |x| = 2 max(x, 0)
+// for the last kDoubledPairs pairs. Both are exact for every finite x (x + |x| is 2x or
+// +0); the first runs on the ALU pipe, the second is one FP32 add with an absolute-value
+// operand on the FMA pipe, so the split balances the two pipes of the epilogue. A doubled
+// chain accumulates exactly twice the partial sums of fma(w, max(x, 0), p) (scaling by 2
+// commutes with rounding for normal floats), and pair_sum halves the pair's sum, again
+// exactly: the scores are those of the plain fixed order.
+constexpr int kDoubledPairs = 3;
+__device__ __forceinline__ float relu_form(float x, int pair) {
+  return pair >= 4 - kDoubledPairs ? x + fabsf(x) : fmaxf(x, 0.f);
+}
+__device__ __forceinline__ float pair_sum(float a, float b, int pair) {
+  return pair >= 4 - kDoubledPairs ? 0.5f * (a + b) : a + b;
 }
 
 // Per-query histogram of appended score keys: one 32-bit counter per bin.
@@ -738,21 +754,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               for (int i = 0; i < 4; ++i) {  // heads 32 half + 8i .. + 7
                 const float4 wa = wv[8 * half + 2 * i];
                 const float4 wb = wv[8 * half + 2 * i + 1];
-                const float r0 = fmaxf(__uint_as_float(x[8 * i + 0]), 0.f);
-                const float r1 = fmaxf(__uint_as_float(x[8 * i + 1]), 0.f);
-                const float r2 = fmaxf(__uint_as_float(x[8 * i + 2]), 0.f);
-                const float r3 = fmaxf(__uint_as_float(x[8 * i + 3]), 0.f);
-                const float r4 = fmaxf(__uint_as_float(x[8 * i + 4]), 0.f);
-                const float r5 = fmaxf(__uint_as_float(x[8 * i + 5]), 0.f);
-                const float r6 = fmaxf(__uint_as_float(x[8 * i + 6]), 0.f);
-                const float r7 = fmaxf(__uint_as_float(x[8 * i + 7]), 0.f);
+                const float r0 = relu_form(__uint_as_float(x[8 * i + 0]), 0);
+                const float r1 = relu_form(__uint_as_float(x[8 * i + 1]), 0);
+                const float r2 = relu_form(__uint_as_float(x[8 * i + 2]), 1);
+                const float r3 = relu_form(__uint_as_float(x[8 * i + 3]), 1);
+                const float r4 = relu_form(__uint_as_float(x[8 * i + 4]), 2);
+                const float r5 = relu_form(__uint_as_float(x[8 * i + 5]), 2);
+                const float r6 = relu_form(__uint_as_float(x[8 * i + 6]), 3);
+                const float r7 = relu_form(__uint_as_float(x[8 * i + 7]), 3);
                 ffma2(ps[0], ps[1], wa.x, wa.y, r0, r1);
                 ffma2(ps[2], ps[3], wa.z, wa.w, r2, r3);
                 ffma2(ps[4], ps[5], wb.x, wb.y, r4, r5);
                 ffma2(ps[6], ps[7], wb.z, wb.w, r6, r7);
               }
             }
-            score = (((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]))) + 0.0f;
+            score = ((pair_sum(ps[0], ps[1], 0) + pair_sum(ps[2], ps[3], 1)) +
+                     (pair_sum(ps[4], ps[5], 2) + pair_sum(ps[6], ps[7], 3))) + 0.0f;
           }
           if (!active) {  // this group reads no columns of the buffer
             tc_fence_before_sync();
