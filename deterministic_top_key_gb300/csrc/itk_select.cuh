@@ -33,7 +33,7 @@ constexpr int kSelThreads = kSelGroups * kSG;
 constexpr int kSelWarps = kSG / 32;           // warps of a group
 constexpr int kSelPer = kCap / kSG;           // candidates a thread holds (entry gtid + kSG r)
 constexpr int kBinsPer = kBins / kSG;         // bins a thread scans in the suffix sums
-static_assert(kSelPer <= 32 && kSelPer % 8 == 0, "candidate masks are 32-bit, runs of 8");
+static_assert(kSelPer <= 32, "candidate masks are 32-bit");
 constexpr int kStageSlack = 256;              // staging slots past top_k
 constexpr int kBigBucket = 32;                // sub-buckets above this size take the full sort
 
@@ -199,15 +199,12 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   unsigned long long vk[kSelPer];  // full 64-bit keys; the score word is the high half
   // entry r of this thread is candidate gtid + kSG r: it exists for r < ceil((n - gtid) / kSG)
   const uint32_t n_mine = n > static_cast<uint32_t>(c.gtid) ? (n - c.gtid + kSG - 1u) / kSG : 0u;
-  const uint32_t valid = n_mine >= 32u ? 0xFFFFFFFFu : (1u << n_mine) - 1u;
 #pragma unroll
   for (int r = 0; r < kSelPer; ++r) vk[r] = 0ull;
 #pragma unroll
-  for (int r0 = 0; r0 < kSelPer; r0 += 8) {  // runs of 8 entries with no bit set are skipped
-    if (((valid >> r0) & 0xFFu) == 0u) continue;
-#pragma unroll
-    for (int r = r0; r < r0 + 8; ++r) {
-      if (!((valid >> r) & 1u)) continue;
+  for (int r = 0; r < kSelPer; ++r) {  // entries past this thread's count are skipped one by one
+    if (r >= static_cast<int>(n_mine)) break;
+    {
       vk[r] = buf[c.gtid + static_cast<uint32_t>(kSG) * r];
     }
   }
@@ -221,11 +218,9 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   }
   gsync(c);
 #pragma unroll
-  for (int r0 = 0; r0 < kSelPer; r0 += 8) {  // runs of 8 entries with no bit set are skipped
-    if (((valid >> r0) & 0xFFu) == 0u) continue;
-#pragma unroll
-    for (int r = r0; r < r0 + 8; ++r) {
-      if (!((valid >> r) & 1u)) continue;
+  for (int r = 0; r < kSelPer; ++r) {  // entries past this thread's count are skipped one by one
+    if (r >= static_cast<int>(n_mine)) break;
+    {
       atomicAdd(&ge[bin_pad(static_cast<uint32_t>(vk[r] >> 32) >> kBinShift)], 1u);
     }
   }
@@ -268,11 +263,9 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   gsync(c);
   uint32_t kept = 0;  // bit r: candidate r lies in a kept bin
 #pragma unroll
-  for (int r0 = 0; r0 < kSelPer; r0 += 8) {  // runs of 8 entries with no bit set are skipped
-    if (((valid >> r0) & 0xFFu) == 0u) continue;
-#pragma unroll
-    for (int r = r0; r < r0 + 8; ++r) {
-      if (!((valid >> r) & 1u)) continue;
+  for (int r = 0; r < kSelPer; ++r) {  // entries past this thread's count are skipped one by one
+    if (r >= static_cast<int>(n_mine)) break;
+    {
       if ((static_cast<uint32_t>(vk[r] >> 32) >> kBinShift) >= tstar) {
         kept |= 1u << r;
         atomicAdd(&sub[sub_pad(sub_bucket(ge, static_cast<uint32_t>(vk[r] >> 32)))], 1u);
@@ -283,10 +276,9 @@ __device__ __forceinline__ void sel_finish(const GroupCtx& c, const unsigned lon
   group_exclusive_scan_padded(c, sub, m_keep);  // sub(i) = first slot of sub-bucket i
   const uint32_t cap = top_k + kStageSlack;
 #pragma unroll
-  for (int r0 = 0; r0 < kSelPer; r0 += 8) {  // runs of 8 entries with no bit set are skipped
-    if (((kept >> r0) & 0xFFu) == 0u) continue;
-#pragma unroll
-    for (int r = r0; r < r0 + 8; ++r) {
+  for (int r = 0; r < kSelPer; ++r) {  // entries past this thread's count are skipped one by one
+    if (r >= static_cast<int>(n_mine)) break;
+    {
       if (!((kept >> r) & 1u)) continue;
       const uint32_t b = sub_bucket(ge, static_cast<uint32_t>(vk[r] >> 32));
       const uint32_t pos = atomicAdd(&sub[sub_pad(b)], 1u);
