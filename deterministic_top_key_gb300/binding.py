@@ -298,7 +298,7 @@ def indexer_topk_bench_hold(n_ctas: int, microseconds: int, stream=None):
 
 
 def indexer_topk_debug_inject(plan, what: int, stream=None):
-    """Test hook (see the header); plan None targets the next no-allocation call (what = 5)."""
+    """Test hook (see the header); plan None targets the next eager or no-allocation call (what = 5)."""
     handle = None if plan is None else plan.handle
     _check(load().indexer_topk_debug_inject(handle, int(what), _stream_handle(stream)))
 

@@ -433,9 +433,9 @@ int read_status_word(uint32_t* d_status, cudaStream_t s, bool* dirty) {
   return fail(ITK_ERR_DEVICE_TIMEOUT, "device status word 0x%x (wait in role %u gave up)", word, (word >> 8) & 0xFFu);
 }
 
-// debug_inject 5 with no plan: the next no-allocation call on this thread runs with the
-// withheld key tile and short wait limit.
-thread_local bool g_noalloc_timeout_next = false;
+// debug_inject 5 with no plan: the next call without a plan (eager or no-allocation) on
+// this thread runs with the withheld key tile and short wait limit.
+thread_local bool g_planless_timeout_next = false;
 
 }  // namespace
 
@@ -607,7 +607,10 @@ int indexer_topk_eager(const itk_desc* desc, const void* q, const void* k, const
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemcpyAsync(blk, host.data(), bl.bytes, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "uploading the eager unit table");
-  return launch_run(L, grid, dev.sm_count, block_tables(L, bl, blk), q, k, w, out_ids, out_scores, workspace, s);
+  RunHooks hooks;
+  hooks.withhold_timeout = g_planless_timeout_next;
+  g_planless_timeout_next = false;
+  return launch_run(L, grid, dev.sm_count, block_tables(L, bl, blk), q, k, w, out_ids, out_scores, workspace, s, hooks);
 }
 
 int indexer_topk_eager_device_status(const itk_desc* desc, void* workspace, size_t workspace_bytes, void* stream) {
@@ -647,7 +650,7 @@ int indexer_topk_device_status(itk_plan plan, void* stream) {
 //   what = 2: write a nonzero value into the plan's two ticket blocks on `stream`, as a
 //             run that stopped midway would leave them.
 //   what = 3 / 4: fixed units per scan CTA / the ticket again.
-//   what = 5: the next run (plan NULL: the next no-allocation call of this thread) has
+//   what = 5: the next run (plan NULL: the next eager or no-allocation call of this thread) has
 //             CTA 0 withhold one key-tile load and every wait limited to kShortWaitCycles,
 //             so that the bounded waits run out and report a timeout.
 int indexer_topk_set_split_event(itk_plan plan, void* event) {
@@ -658,7 +661,7 @@ int indexer_topk_set_split_event(itk_plan plan, void* event) {
 
 int indexer_topk_debug_inject(itk_plan plan, int what, void* stream) {
   if (what == 5 && !plan) {
-    g_noalloc_timeout_next = true;
+    g_planless_timeout_next = true;
     return ITK_OK;
   }
   if (!plan) return fail(ITK_ERR_INVALID_ARGUMENT, "plan is NULL");
@@ -803,8 +806,8 @@ int indexer_topk_run_noalloc(const itk_desc* desc, const void* q, const void* k,
   rc = noalloc_scratch(dev.device, &scratch);
   if (rc) return rc;
   RunHooks hooks;
-  hooks.withhold_timeout = g_noalloc_timeout_next;
-  g_noalloc_timeout_next = false;
+  hooks.withhold_timeout = g_planless_timeout_next;
+  g_planless_timeout_next = false;
   // The tables, then the ticket blocks and status word, which must start at zero: three
   // copies and one memset on the call's stream (the array keeps the previous call's
   // contents otherwise). Working buffers, store and counts need no clearing.

@@ -281,11 +281,11 @@ ITK_API int indexer_topk_noalloc_device_status(void* stream);
  *             units). what = 4 restores the ticket.
  */
 ITK_API int indexer_topk_debug_inject(itk_plan plan, int what, void* stream);
-/*   what = 5: the next run of `plan` -- or, with plan NULL, the next indexer_topk_run_noalloc
- *             call on this thread -- runs with every in-kernel wait limited to about 1 ms
- *             (2^21 SM clocks), and scan CTA 0 withholds the first key-tile load of its
- *             first unit, so that the waits on it run out as a load that never arrives
- *             would make them: the CTA records ITK_ERR_DEVICE_TIMEOUT in the status word,
+/*   what = 5: the next run of `plan` -- or, with plan NULL, the next indexer_topk_eager or
+ *             indexer_topk_run_noalloc call on this thread -- runs with every in-kernel wait
+ *             limited to about 1 ms (2^21 SM clocks), and scan CTA 0 withholds the first
+ *             key-tile load of its first unit, so that the waits on it run out as a load
+ *             that never arrives would make them: the CTA records ITK_ERR_DEVICE_TIMEOUT in the status word,
  *             waits for its own copies and tensor-core work, frees its tensor memory and
  *             returns. The call itself returns ITK_OK with undefined outputs; the status
  *             readers report the timeout, and the next run is correct again. */

@@ -299,3 +299,25 @@ def test_wait_timeout_is_reported_and_the_next_run_is_exact(env, shape):
         parity.assert_exact(ids.cpu().numpy(), sc.cpu().numpy(), r_ids, r_sc)
     plan.device_status()
     plan.destroy()
+
+
+def test_eager_status_reader_reports_a_wait_timeout(env):
+    """The eager entry keeps its status word in the caller's workspace; its reader reports a
+    call whose scan CTA 0 withholds a key-tile load with waits cut to about 1 ms (test
+    hook), and the next eager call with the same workspace is exact again."""
+    binding, torch, dev, wl, (q, k, w), (r_ids, r_sc) = env
+    desc = binding.Desc(wl.T, wl.Tkv, wl.cu_seqlens_q, wl.cu_seqlens_k, wl.top_k)
+    ws = torch.empty(binding.indexer_topk_eager_workspace_bytes(desc), dtype=torch.uint8, device=dev)
+    ids, sc = _bufs(torch, dev, wl)
+    binding.indexer_topk_debug_inject(None, 5)
+    binding.indexer_topk_eager(desc, q, k, w, ids, sc, ws)
+    torch.cuda.synchronize()
+    with pytest.raises(binding.IndexerTopkError) as e:
+        binding.indexer_topk_eager_device_status(desc, ws)
+    assert e.value.status == binding.ITK_ERR_DEVICE_TIMEOUT
+    binding.indexer_topk_eager_device_status(desc, ws)  # reading cleared the word
+    ids.fill_(5)
+    binding.indexer_topk_eager(desc, q, k, w, ids, sc, ws)
+    torch.cuda.synchronize()
+    binding.indexer_topk_eager_device_status(desc, ws)
+    parity.assert_exact(ids.cpu().numpy(), sc.cpu().numpy(), r_ids, r_sc)
