@@ -226,6 +226,44 @@ def test_rechunked_rows_bit_identical(binding, dev):
     np.testing.assert_array_equal(ids0[37:], np.where(ids1[37:] >= 0, ids1[37:] - 800, -1))
 
 
+@pytest.mark.parametrize("kind", ["normal", "int"])
+def test_packed_segments_match_each_segment_alone(binding, dev, kind):
+    """Segment independence: four problems packed as four segments of one call give each
+    problem's rows, with the ids moved by the problem's first key row. The packing changes
+    how the work is cut: alone, the 64-query problem over 24000 keys and the 3-query
+    problem over 9000 keys are split tails (key-split units finished by the merge); packed
+    with the 260-query problem (65 query blocks) nothing is split, and those queries run as
+    filtered and dense units finished by the selection."""
+    top_k = 300
+    parts = [
+        inputs.draw(260, 260, [0, 260], [0, 260], top_k, seed=31, kind=kind),  # direct units
+        inputs.draw(64, 24000, [0, 64], [0, 24000], top_k, seed=32, kind=kind),  # filtered units
+        inputs.draw(3, 9000, [0, 3], [0, 9000], top_k, seed=33, kind=kind),  # one dense unit
+        inputs.draw(5, 7000, [0, 5], [0, 7000], top_k, q_causal_offsets=np.array([100], np.int32), seed=34,
+                    kind=kind),  # explicit offset: 101-105 visible keys
+    ]
+    alone = [run_plan(binding, p, dev) for p in parts]
+    cu_q = np.concatenate([[0], np.cumsum([p.T for p in parts])]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum([p.Tkv for p in parts])]).astype(np.int32)
+    packed = inputs.Workload(
+        "packed", np.concatenate([p.q_bits for p in parts]), np.concatenate([p.k_bits for p in parts]),
+        np.concatenate([p.w for p in parts]), cu_q, cu_k,
+        np.array([p.Tkv - p.T if p.q_causal_offsets is None else int(p.q_causal_offsets[0]) for p in parts],
+                 np.int32), top_k)
+    def split(wl):  # some query block is scanned by more than one unit
+        first_rows = binding.indexer_topk_unit_table(
+            binding.Desc(wl.T, wl.Tkv, wl.cu_seqlens_q, wl.cu_seqlens_k, top_k, wl.q_causal_offsets))[:, 0]
+        return len(np.unique(first_rows)) < len(first_rows)
+
+    assert [split(p) for p in parts] == [False, True, True, False]
+    assert not split(packed)
+    ids, sc = run_plan(binding, packed, dev)
+    for i, (a_ids, a_sc) in enumerate(alone):
+        rows = slice(cu_q[i], cu_q[i + 1])
+        np.testing.assert_array_equal(sc[rows].view(np.uint32), a_sc.view(np.uint32))
+        np.testing.assert_array_equal(np.where(ids[rows] >= 0, ids[rows] - cu_k[i], -1), a_ids)
+
+
 def test_eager_matches_prepared(binding, dev):
     import torch
 
