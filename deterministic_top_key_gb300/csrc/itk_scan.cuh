@@ -26,12 +26,17 @@
 //
 // Score arithmetic (fixed, so a score depends only on q[t], k[s] and w[t], never on
 // tiling, unit or CTA): the tensor core forms the FP32 dot products x_h = q[t,h,:].k[s,:]
-// over D = 128 in eight K = 16 steps in a fixed order; the epilogue thread that owns key
-// s keeps eight partial sums p_m (m = 0..7), p_m = fma(w[t,h], max(x_h, 0), p_m) over
-// h = m, m+8, ..., m+56 in that order, and returns
+// over D = 128 in eight K = 16 steps in a fixed order; the epilogue forms eight partial
+// sums p_m (m = 0..7), p_m = fma(w[t,h], max(x_h, 0), p_m) over h = m, m+8, ..., m+56 in
+// that order, and returns
 //     ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7)) + 0
-// (the "+ 0" turns a -0 into +0). Chains 2..7 are evaluated on doubled values (relu_form,
-// pair_sum below) to share the work between two pipes; the result is the same bits.
+// (the "+ 0" turns a -0 into +0). The four threads of a quad share four keys: thread c
+// (c = 0..3) holds the head columns of chains 2c and 2c + 1 of all four (one 16x256b
+// tensor-memory load per half of the warp's 32 keys) and keeps the head weights of those
+// chains in registers; it forms P_c = p_2c + p_2c+1 for each key, and two shuffle rounds
+// over the quad add (P0 + P1) + (P2 + P3), leaving key c's score with thread c. Each FMA
+// is evaluated as fma(w/2, x + |x|, p) (relu_fma below): the same exact product, so the
+// same bits, with the ReLU as one add on the FMA pipe.
 //
 // Candidate filter: a query's working buffer holds keys whose score key lies in a bin
 // (top 11 bits of the order-preserving score key) at or above a threshold bin; the
@@ -141,19 +146,14 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
-// ReLU of the chains of pair j (chains 2j and 2j + 1): max(x, 0), or x + |x| = 2 max(x, 0)
-// for the last kDoubledPairs pairs. Both are exact for every finite x (x + |x| is 2x or
-// +0); the first runs on the ALU pipe, the second is one FP32 add with an absolute-value
-// operand on the FMA pipe, so the split balances the two pipes of the epilogue. A doubled
-// chain accumulates exactly twice the partial sums of fma(w, max(x, 0), p) (scaling by 2
-// commutes with rounding for normal floats), and pair_sum halves the pair's sum, again
-// exactly: the scores are those of the plain fixed order.
-constexpr int kDoubledPairs = 3;
-__device__ __forceinline__ float relu_form(float x, int pair) {
-  return pair >= 4 - kDoubledPairs ? x + fabsf(x) : fmaxf(x, 0.f);
-}
-__device__ __forceinline__ float pair_sum(float a, float b, int pair) {
-  return pair >= 4 - kDoubledPairs ? 0.5f * (a + b) : a + b;
+// One step of two head chains, (p0, p1) = (fma(w0, max(x0, 0), p0), fma(w1, max(x1, 0), p1)),
+// given the halved weights hw = w / 2: x + |x| is 2 max(x, 0) exactly for every finite x
+// (2x or +0), so hw (x + |x|) is the exact product w max(x, 0) whenever w / 2 is exact
+// (w = 0 or |w| >= 2^-125), and each fused multiply-add rounds the same exact value as the
+// plain form. The ReLU becomes one FP32 add with an absolute-value operand, on the FMA
+// pipe (a max runs on the ALU pipe at half rate).
+__device__ __forceinline__ void relu_fma2(float& p0, float& p1, float hw0, float hw1, float x0, float x1) {
+  ffma2(p0, p1, hw0, hw1, x0 + fabsf(x0), x1 + fabsf(x1));
 }
 
 // Per-query histogram of appended score keys: one 32-bit counter per bin.
@@ -638,14 +638,19 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     c.radix = reinterpret_cast<uint32_t*>(smem + kOffRadix) + 256 * g;
     c.sel = reinterpret_cast<uint32_t*>(smem + kOffSel) + 8 * g;
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
-    const int key_lane = quarter * 32 + lane;
+    // quad layout: thread (qd, qc) = (lane / 4, lane % 4) reads the head columns 8j + 2 qc
+    // and 8j + 2 qc + 1 (j = 0..7) of the key rows qd and qd + 8 of each half (16 rows) of
+    // the quarter, and after the quad's reduction owns key qc of its four: half qc / 2,
+    // row qd + 8 (qc % 2)
+    const int qd = lane >> 2, qc = lane & 3;
+    const int key_lane = quarter * 32 + 16 * (qc >> 1) + 8 * (qc & 1) + qd;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    float hw[16];  // the halved weights of this thread's chains: hw[2j + e] = w[t, 8j + 2 qc + e] / 2
     const uint32_t K = static_cast<uint32_t>(p.top_k);
     const uint64_t pol_cand = policy_evict_last();   // working buffers: reused unit after unit
     const uint64_t pol_store = policy_evict_first();  // candidate store: read only by the next kernel
     uint32_t* hist_g = reinterpret_cast<uint32_t*>(smem + kOffHist) + g * kBins;
     uint32_t* qs = s_qs + g * 4;
-    const float4* wv = reinterpret_cast<const float4*>(s_w + g * kHeads);
     unsigned long long* cand = p.cand + static_cast<size_t>(blockIdx.x) * kCandKeysPerCta + static_cast<size_t>(g) * kQCap;
     unsigned long long* exact_scratch =
         p.cand + static_cast<size_t>(blockIdx.x) * kCandKeysPerCta + static_cast<size_t>(kQB) * kQCap + g * kMaxTopK;
@@ -690,6 +695,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       // kQCap keys before its first sync point)
       if (c.gtid < 4) qs[c.gtid] = (c.gtid == 0 && active) ? static_cast<uint32_t>(min(max(mine, 0), kQCap)) : 0u;
       gsync(c);
+  #pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float2 wp = *reinterpret_cast<const float2*>(s_w + g * kHeads + 8 * j + 2 * qc);
+        hw[2 * j] = 0.5f * wp.x;
+        hw[2 * j + 1] = 0.5f * wp.y;
+      }
       // The tile loop, compiled for three kinds of unit: direct (every visible key to the
       // store), dense (every visible key to the working buffer, no sync points) and
       // filtered (threshold raised at sync points).
@@ -737,39 +748,36 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           float score = 0.f;
           if (active) {
             const uint32_t col = static_cast<uint32_t>(ab * kN + g * kHeads);
-            float ps[8];
+            float P[4];  // P_qc of the quad's keys: [2 half] row qd, [2 half + 1] row qd + 8
   #pragma unroll
-            for (int m = 0; m < 8; ++m) ps[m] = 0.f;
-  #pragma unroll
-            for (int half = 0; half < 2; ++half) {  // heads 32 half .. 32 half + 31
+            for (int half = 0; half < 2; ++half) {  // key rows 16 half .. 16 half + 15 of the quarter
               uint32_t x[32];
-              tmem_ld32(lane_addr + col + 32 * half, x);
+              tmem_ld16x256b_x8(lane_addr + (static_cast<uint32_t>(16 * half) << 16) + col, x);
               tmem_ld_wait();
               if (half == 1) {  // every column is in registers: hand the accumulator back now
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bars.ae(ab));
               }
+              float pa0 = 0.f, pa1 = 0.f, pb0 = 0.f, pb1 = 0.f;
   #pragma unroll
-              for (int i = 0; i < 4; ++i) {  // heads 32 half + 8i .. + 7
-                const float4 wa = wv[8 * half + 2 * i];
-                const float4 wb = wv[8 * half + 2 * i + 1];
-                const float r0 = relu_form(__uint_as_float(x[8 * i + 0]), 0);
-                const float r1 = relu_form(__uint_as_float(x[8 * i + 1]), 0);
-                const float r2 = relu_form(__uint_as_float(x[8 * i + 2]), 1);
-                const float r3 = relu_form(__uint_as_float(x[8 * i + 3]), 1);
-                const float r4 = relu_form(__uint_as_float(x[8 * i + 4]), 2);
-                const float r5 = relu_form(__uint_as_float(x[8 * i + 5]), 2);
-                const float r6 = relu_form(__uint_as_float(x[8 * i + 6]), 3);
-                const float r7 = relu_form(__uint_as_float(x[8 * i + 7]), 3);
-                ffma2(ps[0], ps[1], wa.x, wa.y, r0, r1);
-                ffma2(ps[2], ps[3], wa.z, wa.w, r2, r3);
-                ffma2(ps[4], ps[5], wb.x, wb.y, r4, r5);
-                ffma2(ps[6], ps[7], wb.z, wb.w, r6, r7);
+              for (int j = 0; j < 8; ++j) {  // heads 8j + 2 qc and 8j + 2 qc + 1
+                relu_fma2(pa0, pa1, hw[2 * j], hw[2 * j + 1], __uint_as_float(x[4 * j + 0]),
+                          __uint_as_float(x[4 * j + 1]));
+                relu_fma2(pb0, pb1, hw[2 * j], hw[2 * j + 1], __uint_as_float(x[4 * j + 2]),
+                          __uint_as_float(x[4 * j + 3]));
               }
+              P[2 * half] = pa0 + pa1;
+              P[2 * half + 1] = pb0 + pb1;
             }
-            score = ((pair_sum(ps[0], ps[1], 0) + pair_sum(ps[2], ps[3], 1)) +
-                     (pair_sum(ps[4], ps[5], 2) + pair_sum(ps[6], ps[7], 3))) + 0.0f;
+            // (P0 + P1) + (P2 + P3) over the quad; a + b and b + a are the same bits, so each
+            // key's sum is the fixed tree whichever thread adds it. Round 1 (threads c, c ^ 1):
+            // keep the keys k with k % 2 == c % 2. Round 2 (c, c ^ 2): keep key c.
+            const bool odd = (qc & 1) != 0;
+            const float q0 = (odd ? P[1] : P[0]) + __shfl_xor_sync(0xFFFFFFFFu, odd ? P[0] : P[1], 1);
+            const float q1 = (odd ? P[3] : P[2]) + __shfl_xor_sync(0xFFFFFFFFu, odd ? P[2] : P[3], 1);
+            const bool hi = (qc & 2) != 0;
+            score = ((hi ? q1 : q0) + __shfl_xor_sync(0xFFFFFFFFu, hi ? q0 : q1, 2)) + 0.0f;
           }
           if (!active) {  // this group reads no columns of the buffer
             tc_fence_before_sync();
