@@ -88,6 +88,20 @@ def test_default_offsets_bottom_right(binding, dev, oracle_mod):
     parity.assert_exact(ids, sc, r_ids, r_sc)
 
 
+def test_weights_down_to_two_to_the_minus_125_are_exact(binding, dev, oracle_mod):
+    """The epilogue multiplies w / 2 by x + |x|; halving is exact for |w| >= 2^-125, so
+    integer q and k with weights in {0, +-2^-125, +-2^-124} (every product and sum an exact
+    multiple of 2^-125 below 2^-100) give the oracle's bits."""
+    wl = inputs.draw(300, 700, [0, 300], [0, 700], 200, seed=41, kind="int")
+    rng = np.random.default_rng(41)
+    tiny = np.float32(2.0 ** -125)
+    w = (rng.choice(np.array([-2, -1, 0, 1, 2], np.float32), size=wl.w.shape) * tiny).astype(np.float32)
+    wl = inputs.Workload("tiny-w", wl.q_bits, wl.k_bits, w, wl.cu_seqlens_q, wl.cu_seqlens_k, None, wl.top_k)
+    ids, sc = run_plan(binding, wl, dev)
+    r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl))
+    parity.assert_exact(ids, sc, r_ids, r_sc)
+
+
 @pytest.mark.parametrize("top_k", [1, 3, 128, 2048])
 def test_top_k_values(binding, dev, oracle_mod, top_k):
     wl = inputs.draw(70, 2100, [0, 70], [0, 2100], top_k, seed=2, kind="int")
