@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import subprocess
@@ -38,11 +39,19 @@ KERNEL_SOURCES = [os.path.join(ROOT, "deterministic_top_key_gb300", "csrc", f)
                   for f in ("itk_common.cuh", "itk_scan.cuh", "itk_ptx.cuh")]
 
 
+def _code_only(text: str) -> str:
+    """The source without its comments and with whitespace collapsed: a comment-only edit
+    does not change the compiled kernel, so it keeps the recorded traffic."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -738,6 +738,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               thr_f = thr < 4u ? -__int_as_float(0x7F800000) : key_to_float(thr << kBinShift);
             }
           }
+          // The warp enters this wait converged (every branch above is uniform or closes
+          // before it), so each try_wait, abort-flag read and clock read of the wait is one
+          // instruction for all 32 lanes and returns them the same value: the warp leaves
+          // the wait as one, as the warp-wide tensor-memory loads and shuffles below need.
           if (!mbar_wait(bars.af(ab), (ac >> 1) & 1, s_abort, p.wait_limit)) {
             record_timeout(p.status, s_abort, 10);
             atomicOr(&s_gfail[g], 1u);  // the group leaves at its next sync point
