@@ -329,6 +329,22 @@ def test_split_tail_with_fewer_keys_than_top_k(binding, dev, oracle_mod, kind):
     assert (ids[:, 1500:] == -1).all()
 
 
+@pytest.mark.parametrize("kind", ["int", "normal"])
+def test_split_tail_at_the_chunk_budget(binding, dev, oracle_mod, kind):
+    """Four queries over 200000 keys: the one query block is split into the whole budget of
+    256 key-range units (6-7 tiles each), and the merge selects each row from 256 candidate
+    lists (about 200 K keys per query)."""
+    wl = inputs.draw(4, 200000, [0, 4], [0, 200000], 2048, seed=44, kind=kind)
+    units = binding.indexer_topk_unit_table(binding.Desc(4, 200000, [0, 4], [0, 200000], 2048))
+    assert len(units) == 256 and (units[:, 0] == 0).all()
+    ids, sc = run_plan(binding, wl, dev)
+    if kind == "int":
+        r_ids, r_sc = oracle_mod.topk(parity.oracle_problem(wl))
+        parity.assert_exact(ids, sc, r_ids, r_sc)
+    else:
+        parity.assert_close(ids, sc, wl, np.arange(4))
+
+
 def test_eager_matches_prepared_on_a_split_tail(binding, dev):
     """The eager entry runs the same launches (the scan, then the merge) for a split tail."""
     import torch
